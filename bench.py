@@ -1,0 +1,349 @@
+"""Benchmark: causal linear-attention forward (phi = elu + 1) tokens/s on GB300.
+
+One step = one la_causal_fwd call (every kernel of the causal path) over one
+batch of the causal B=8 H=8 N=3072 D=64 bf16 workload (a 32x32x3 pixel-channel
+sequence), inputs resident in device memory. Input sets rotate so that the
+bytes touched between two reads of one set exceed the L2 cache.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the float64 CPU
+oracle on the same workload instead (a deliberately slow baseline).
+Multi-GPU (torchrun): every rank runs its own batch (heads are independent,
+no collective on the data path), timing is the max over ranks.
+"""
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, make_workload, to_f64  # noqa: E402
+
+METRIC = "causal linear-attn fwd tokens/s (B·H·N/s) & % of HBM/tensor roofline, 1 GB300"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="image", choices=["image", "long"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def alg_bytes(w):
+    """Algorithmic bytes of one forward: read q, k, v and write o once."""
+    elem = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * w.N * (3 * w.D + w.D) * elem
+
+
+def csrc_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "linear_attention_elu_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from an ncu capture, if taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(key)
+        if rec and rec.get("csrc_digest") == csrc_digest():
+            return rec["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return None
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w, budget_s=10.0):
+    """Times the float64 oracle (recurrent form) on whole heads of the workload."""
+    import oracle
+    q, k, v = make_workload(w, seed=0)
+    BH = w.B * w.H
+    qf, kf, vf = (to_f64(t).reshape(BH, w.N, w.D) for t in (q, k, v))
+    threads = oracle.default_threads()
+    heads, elapsed, n = 0, 0.0, 1
+    while elapsed < budget_s and heads < BH:
+        n = min(n, BH - heads)
+        t0 = time.perf_counter()
+        oracle.recurrent(qf[heads:heads + n], kf[heads:heads + n], vf[heads:heads + n], True,
+                         nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        heads += n
+        n *= 2
+    return {"value": heads * w.N / elapsed, "unit": UNIT, "cores": min(threads, BH),
+            "kind": "oracle",
+            "sample": f"{heads} of {BH} heads x {w.N} tokens, float64 recurrent form, "
+                      f"{elapsed:.2f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    q, k, v = make_workload(w, seed=0)
+    BH = w.B * w.H
+    qf, kf, vf = (to_f64(t).reshape(BH, w.N, w.D) for t in (q, k, v))
+    threads = oracle.default_threads()
+    sample_heads = max(1, min(BH, threads))  # one head per core per step
+
+    def step(i):
+        h0 = (i * sample_heads) % BH
+        idx = [(h0 + j) % BH for j in range(sample_heads)]
+        oracle.recurrent(qf[idx], kf[idx], vf[idx], True, nthreads=threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps * sample_heads * w.N / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, sample_heads),
+                         "kind": "oracle",
+                         "sample": f"each step: {sample_heads} of {BH} heads x {w.N} tokens, "
+                                   "float64 recurrent form"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import linear_attention_elu_gb300 as la
+
+    # Inputs: R independent sets so the sets touched between two uses of one set exceed L2.
+    per_set = alg_bytes(w)
+    R = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    sets = []
+    for r in range(R):
+        q, k, v = make_workload(w, seed=rank * 1000 + r)
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(v, device=dev)))
+    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, sets[0][0].dtype, dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = la.la_launch_count(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D,
+                                           sets[0][0].dtype)
+
+    def step(i):
+        q, k, v, o = sets[i % R]
+        la.la_causal_fwd(q, k, v, o=o, ws=ws)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    status = la.la_query_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status after timed region: {la.la_status_string(status)}")
+    ms_per_step = ms / args.steps
+    tokens = w.tokens * world
+    value = tokens / (ms_per_step * 1e-3)
+
+    # Dominant-kernel duration: per-call events over the same rotation (one call = the path).
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # End to end: pinned host inputs -> device, forward, result -> pinned host.
+    hq, hk, hv = (t.cpu().pin_memory() for t in make_workload(w, seed=rank * 1000 + 77))
+    ho = torch.empty_like(hv).pin_memory()
+    dq, dk, dv, do = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, ho))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        la.la_causal_fwd(dq, dk, dv, o=do, ws=ws)
+        ho.copy_(do, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+
+    hbm, src = peaks()
+    achieved = alg_bytes(w) / (call_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Dk": w.D, "Dv": w.D,
+                   "eps": 1e-6, "state_dtype": "f32",
+                   "l2": f"{R} rotating input sets of {per_set / 1e6:.1f} MB (> L2 between reuses)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if src == "measured" else "fallback 6.8 TB/s",
+                     "traffic": recorded_traffic(f"causal:{args.workload}"),
+                     "kernel": f"la_causal_fwd ({launches_per_step} launches per call)",
+                     "alg_bytes_per_launch": alg_bytes(w), "avg_call_ms": call_ms},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

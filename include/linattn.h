@@ -1,0 +1,143 @@
+/*
+ * linattn.h — C ABI of the GB300 (sm_103a) kernels for kernelized linear
+ * attention with the feature map phi(x) = elu(x) + 1.
+ *
+ * Definitions this library computes (all per (b, h) head, rows i = 1..N):
+ *
+ *   phi(x)  = x + 1 for x > 0, exp(x) for x <= 0, element-wise
+ *             ("Why Replace Attention? The Softmax Bottleneck and the Path to
+ *              Linear Time", section 5.3; "Transformers Are RNNs: Linear
+ *              Attention", "Factor the Similarity Kernel").
+ *   non-causal:  S = sum_j phi(k_j) v_j^T,  z = sum_j phi(k_j),
+ *                o_i = phi(q_i)^T S / (phi(q_i)^T z + eps)
+ *             ("Transformers Are RNNs: Linear Attention", "Reassociate the
+ *              Products"; "Why Replace Attention? ...", section 6.2;
+ *              "Linear Attention" research-hub note, the matrix form
+ *              O = (phi(Q)(phi(K)^T V)) / (phi(Q)(phi(K)^T 1))).
+ *   causal:      S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j),
+ *                o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i + eps)
+ *             ("Why Replace Attention? ...", sections 7.1-7.2;
+ *              "[Paper Review] Transformers are RNNs ...", section 3.4).
+ *   decode step: S <- S + phi(k) v^T, z <- z + phi(k), then
+ *                o = phi(q)^T S / (phi(q)^T z + eps)   (update, then read)
+ *             ("Transformers Are RNNs: Linear Attention", "Turn Causal
+ *              Attention into a Recurrence"; "Why Replace Attention? ...",
+ *              section 7.2, steps 1-4).
+ *
+ * eps is added once to the scalar denominator (the pages ask for an epsilon
+ * without fixing its value or place; 1e-6 is the customary value).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are contiguous, row-major [B, H, N, D] with D innermost
+ *    (decode: [B, H, D]). q and k have Dk columns, v and o have Dv columns.
+ *    o has the input dtype. S is [B, H, Dk, Dv] float32 (row = feature index,
+ *    column = value index) and z is [B, H, Dk] float32.
+ *  - All pointers except the host-side `bytes` out-parameter are DEVICE
+ *    pointers owned by the caller. The library allocates no memory and keeps
+ *    no global state; per-call scratch lives in the caller's workspace.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream). Argument errors are reported synchronously by the return
+ *    value and nothing is launched. A launch failure returns LA_ERR_CUDA.
+ *    A bounded device-side wait that expires sets the workspace status word;
+ *    la_query_status() reports it as LA_ERR_TIMEOUT.
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* la_stream_t;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad dtype/op     */
+    LA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. Dk > 128)         */
+    LA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned        */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed       */
+    LA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (see status)   */
+} la_status;
+
+typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2 } la_op;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* la_status_string(la_status s);
+
+/* Library ABI version, (major << 16) | minor. */
+uint32_t la_version(void);
+
+/*
+ * Workspace bytes needed by `op` for this shape and dtype (0 for
+ * LA_OP_DECODE, which needs none). `bytes` is a HOST pointer. The workspace
+ * must be 256-byte aligned and, before its first use, prepared once with
+ * la_workspace_init(); afterwards the library keeps it consistent across
+ * calls. A workspace may be reused by any later call on the same stream;
+ * calls that overlap in time must use distinct workspaces.
+ */
+la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
+                            size_t* bytes);
+
+/*
+ * Number of kernel launches one call of `op` makes for this shape and dtype
+ * (host-only query; `launches` is a HOST pointer). Useful for stream and
+ * graph planning and for counting launches in a timed region.
+ */
+la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
+                          int* launches);
+
+/* Zero-fills the workspace header and sets the default wait limit (async on stream). */
+la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * Non-causal forward: o_i = phi(q_i)^T S / (phi(q_i)^T z + eps) with
+ * S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j) over all j of the head.
+ * q, k: [B,H,N,Dk]; v, o: [B,H,N,Dv]; dtype dt for all four.
+ * Supported: LA_F32 with 1 <= Dk, Dv <= 128; LA_BF16 with the same range
+ * (Dk = Dv in {64, 128} use the tensor-core path).
+ */
+la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
+                           int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                           void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * Causal forward: o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i + eps) with the
+ * inclusive prefix sums S_i, z_i. Shapes and dtypes as la_noncausal_fwd.
+ * S_out [B,H,Dk,Dv] and z_out [B,H,Dk] (float32, nullable) receive the final
+ * state S_N, z_N, so that la_decode_step can continue the sequence.
+ */
+la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
+                        int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                        float* S_out, float* z_out,
+                        void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * One recurrent decode step for B*H independent heads, in place:
+ * S <- S + phi(k) v^T, z <- z + phi(k), o = phi(q)^T S / (phi(q)^T z + eps).
+ * q, k: [B,H,Dk]; v, o: [B,H,Dv] in dtype dt; S: [B,H,Dk,Dv] and z: [B,H,Dk]
+ * float32, read and written. A fresh sequence starts from S = 0, z = 0
+ * (caller zero-fills). Needs no workspace. S must be 16-byte aligned.
+ */
+la_status la_decode_step(const void* q, const void* k, const void* v, void* o,
+                         float* S, float* z, int B, int H, int Dk, int Dv, la_dtype dt,
+                         float eps, la_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the workspace status word.
+ * Returns LA_OK, LA_ERR_TIMEOUT (a bounded wait expired in an earlier call
+ * that used this workspace) or LA_ERR_CUDA.
+ */
+la_status la_query_status(void* workspace, la_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

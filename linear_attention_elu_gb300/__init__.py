@@ -1,0 +1,205 @@
+"""Python binding of liblinattn.so (kernelized linear attention, phi = elu + 1).
+
+Argument marshalling only: every function here checks shapes and dtypes,
+passes raw device pointers and the current CUDA stream to the C ABI declared
+in include/linattn.h, and raises on a non-OK status. All arithmetic runs in
+the library's CUDA kernels; there is no other code path. PyTorch supplies
+device memory and streams.
+
+Importing the package loads the library and fails loudly if it has not been
+built (``python linear_attention_elu_gb300/build.py``).
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "LA_F32", "LA_BF16", "LA_OP_NONCAUSAL", "LA_OP_CAUSAL", "LA_OP_DECODE", "LinAttnError",
+    "la_status_string", "la_version", "la_workspace_size", "la_launch_count", "la_workspace_init",
+    "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
+    "library_path",
+]
+
+LA_F32, LA_BF16 = 0, 1
+LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE = 0, 1, 2
+LA_OK, LA_ERR_TIMEOUT = 0, 5
+
+_DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {la_status_string(status)}")
+
+
+def library_path():
+    return _build.LIB
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"liblinattn.so is not built ({path}); run `python linear_attention_elu_gb300/build.py`"
+            " or __graft_entry__.build(). There is no fallback implementation.")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.la_status_string.argtypes = [I]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_version.argtypes = []
+    lib.la_version.restype = ctypes.c_uint32
+    lib.la_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(Z)]
+    lib.la_workspace_size.restype = I
+    lib.la_launch_count.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I)]
+    lib.la_launch_count.restype = I
+    lib.la_workspace_init.argtypes = [P, Z, P]
+    lib.la_workspace_init.restype = I
+    lib.la_noncausal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, Z, P]
+    lib.la_noncausal_fwd.restype = I
+    lib.la_causal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P]
+    lib.la_causal_fwd.restype = I
+    lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+    lib.la_decode_step.restype = I
+    lib.la_query_status.argtypes = [P, P]
+    lib.la_query_status.restype = I
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status, where):
+    if status != LA_OK:
+        raise LinAttnError(status, where)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _dt(t):
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+    return _DTYPES[t.dtype]
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous ([B, H, N, D], D innermost)")
+
+
+def la_status_string(status):
+    return _lib.la_status_string(int(status)).decode()
+
+
+def la_version():
+    return int(_lib.la_version())
+
+
+def la_workspace_size(op, B, H, N, Dk, Dv, dtype):
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    n = ctypes.c_size_t(0)
+    _check(_lib.la_workspace_size(int(op), B, H, N, Dk, Dv, dt, ctypes.byref(n)),
+           "la_workspace_size")
+    return int(n.value)
+
+
+def la_launch_count(op, B, H, N, Dk, Dv, dtype):
+    """Kernel launches one call of `op` makes at this shape (host-only query)."""
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    n = ctypes.c_int(0)
+    _check(_lib.la_launch_count(int(op), B, H, N, Dk, Dv, dt, ctypes.byref(n)), "la_launch_count")
+    return int(n.value)
+
+
+def la_workspace_init(ws, stream=None):
+    _need_cuda(ws)
+    _check(_lib.la_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "la_workspace_init")
+    return ws
+
+
+def workspace(op, B, H, N, Dk, Dv, dtype, device=None, stream=None):
+    """Allocates (through PyTorch) and initialises a workspace for `op` at this shape."""
+    n = la_workspace_size(op, B, H, N, Dk, Dv, dtype)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+    return la_workspace_init(ws, stream)
+
+
+def _shape4(q, k, v):
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"expected q, k [B,H,N,Dk] and v [B,H,N,Dv]; got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    B, H, N, Dk = q.shape
+    return B, H, N, Dk, v.shape[3]
+
+
+def la_noncausal_fwd(q, k, v, o=None, eps=1e-6, ws=None, stream=None):
+    """o_i = phi(q_i)^T S / (phi(q_i)^T z + eps), S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j)."""
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, ws)
+    if ws is None:
+        ws = workspace(LA_OP_NONCAUSAL, B, H, N, Dk, Dv, q.dtype, q.device, stream)
+    _check(_lib.la_noncausal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                                 float(eps), _ptr(ws), ws.numel(), _stream(stream)),
+           "la_noncausal_fwd")
+    return o
+
+
+def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, stream=None):
+    """Causal o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i + eps); optional final state out (fp32)."""
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, ws, S_out, z_out)
+    for t, shp in ((S_out, (B, H, Dk, Dv)), (z_out, (B, H, Dk))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
+            raise ValueError(f"state outputs must be float32 with shape {shp}")
+    if ws is None:
+        ws = workspace(LA_OP_CAUSAL, B, H, N, Dk, Dv, q.dtype, q.device, stream)
+    _check(_lib.la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                              float(eps), _ptr(S_out), _ptr(z_out), _ptr(ws), ws.numel(),
+                              _stream(stream)),
+           "la_causal_fwd")
+    return o
+
+
+def la_decode_step(q, k, v, S, z, o=None, eps=1e-6, stream=None):
+    """One recurrent step on (S, z) in place; q, k [B,H,Dk], v [B,H,Dv]; returns o [B,H,Dv]."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,Dk] and v [B,H,Dv]")
+    B, H, Dk = q.shape
+    Dv = v.shape[2]
+    if S.dtype != torch.float32 or z.dtype != torch.float32 or tuple(S.shape) != (B, H, Dk, Dv) \
+            or tuple(z.shape) != (B, H, Dk):
+        raise ValueError("S must be float32 [B,H,Dk,Dv] and z float32 [B,H,Dk]")
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, S, z)
+    _check(_lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H, Dk,
+                               Dv, _dt(q), float(eps), _stream(stream)),
+           "la_decode_step")
+    return o
+
+
+def la_query_status(ws, stream=None):
+    """Synchronises the stream and returns (and clears) the workspace status code."""
+    return int(_lib.la_query_status(_ptr(ws), _stream(stream)))

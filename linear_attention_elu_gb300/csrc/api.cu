@@ -1,0 +1,206 @@
+// C-ABI entry points (declared in include/linattn.h): argument checks,
+// workspace layout, path choice and launches. No entry point allocates
+// device memory; every buffer belongs to the caller.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using la::WsHeader;
+
+namespace {
+
+constexpr size_t kHeaderBytes = sizeof(WsHeader);
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+la_status check_common(int B, int H, int N, int Dk, int Dv, la_dtype dt) {
+    if (B < 0 || H < 0 || N < 0) return LA_ERR_INVALID_ARG;
+    if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_INVALID_ARG;
+    if (Dk <= 0 || Dv <= 0) return LA_ERR_INVALID_ARG;
+    if (Dk > la::kMaxDim || Dv > la::kMaxDim) return LA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535) return LA_ERR_UNSUPPORTED;  // heads map to grid.y
+    return LA_OK;
+}
+
+la_status check_tensor(const void* p, int64_t elems, la_dtype dt) {
+    if (elems == 0) return LA_OK;
+    if (!p) return LA_ERR_INVALID_ARG;
+    if (!aligned(p, 16)) return LA_ERR_INVALID_ARG;
+    (void)dt;
+    return LA_OK;
+}
+
+la_status check_eps(float eps) {
+    return (isfinite(eps) && eps >= 0.f) ? LA_OK : LA_ERR_INVALID_ARG;
+}
+
+size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
+    const int64_t BH = (int64_t)B * H;
+    (void)dt;
+    if (BH == 0 || N == 0) return 0;
+    switch (op) {
+        case LA_OP_CAUSAL:
+            return la::simt_causal_workspace(BH, N, Dk, Dv);
+        case LA_OP_NONCAUSAL:
+            return la::simt_noncausal_workspace(BH, N, Dk, Dv);
+        default:
+            return 0;
+    }
+}
+
+la_status check_workspace(void* ws, size_t have, size_t need) {
+    if (need == 0) return LA_OK;
+    if (!ws || !aligned(ws, 256) || have < need) return LA_ERR_WORKSPACE;
+    return LA_OK;
+}
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+__global__ void init_header_kernel(WsHeader* h) {
+    h->status = 0;
+    h->epoch = 0;
+    h->ticket = 0;
+    h->done = 0;
+    h->max_spin = la::kDefaultMaxSpin;
+    h->hold_item = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* la_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: shape or dtype not supported";
+        case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime error";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait expired";
+    }
+    return "unknown la_status";
+}
+
+uint32_t la_version(void) { return (0u << 16) | 1u; }
+
+la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
+                            size_t* bytes) {
+    if (!bytes) return LA_ERR_INVALID_ARG;
+    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE)
+        return LA_ERR_INVALID_ARG;
+    la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if (op == LA_OP_DECODE) {
+        *bytes = 0;
+        return LA_OK;
+    }
+    *bytes = kHeaderBytes + round_up(body_bytes(op, B, H, N, Dk, Dv, dt), 256);
+    return LA_OK;
+}
+
+la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
+                          int* launches) {
+    if (!launches) return LA_ERR_INVALID_ARG;
+    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE)
+        return LA_ERR_INVALID_ARG;
+    la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0 || (op != LA_OP_DECODE && N == 0)) {
+        *launches = 0;
+        return LA_OK;
+    }
+    *launches = op == LA_OP_DECODE ? 1 : 3;
+    return LA_OK;
+}
+
+la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t stream) {
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < kHeaderBytes)
+        return LA_ERR_WORKSPACE;
+    init_header_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((WsHeader*)workspace);
+    return from_cuda(cudaPeekAtLastError());
+}
+
+la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
+                           int N, int Dk, int Dv, la_dtype dt, float eps, void* workspace,
+                           size_t workspace_bytes, la_stream_t stream) {
+    la_status s = check_common(B, H, N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if ((s = check_eps(eps)) != LA_OK) return s;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t rows = BH * N;
+    if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
+        (s = check_tensor(v, rows * Dv, dt)) || (s = check_tensor(o, rows * Dv, dt)))
+        return s;
+    if (rows == 0) return LA_OK;
+    const size_t need = kHeaderBytes + body_bytes(LA_OP_NONCAUSAL, B, H, N, Dk, Dv, dt);
+    if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
+    char* body = (char*)workspace + kHeaderBytes;
+    return from_cuda(la::simt_noncausal(q, k, v, o, dt, BH, N, Dk, Dv, eps, body,
+                                        (cudaStream_t)stream));
+}
+
+la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
+                        int N, int Dk, int Dv, la_dtype dt, float eps, float* S_out,
+                        float* z_out, void* workspace, size_t workspace_bytes,
+                        la_stream_t stream) {
+    la_status s = check_common(B, H, N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if ((s = check_eps(eps)) != LA_OK) return s;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t rows = BH * N;
+    if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
+        (s = check_tensor(v, rows * Dv, dt)) || (s = check_tensor(o, rows * Dv, dt)))
+        return s;
+    if ((S_out && !aligned(S_out, 16)) || (z_out && !aligned(z_out, 16)))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (BH == 0) return LA_OK;
+    if (N == 0) {
+        // Empty sequence: the final state is the empty sum.
+        if (S_out && cudaMemsetAsync(S_out, 0, sizeof(float) * BH * Dk * Dv, st))
+            return LA_ERR_CUDA;
+        if (z_out && cudaMemsetAsync(z_out, 0, sizeof(float) * BH * Dk, st)) return LA_ERR_CUDA;
+        return LA_OK;
+    }
+    const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL, B, H, N, Dk, Dv, dt);
+    if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
+    char* body = (char*)workspace + kHeaderBytes;
+    return from_cuda(
+        la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, S_out, z_out, body, st));
+}
+
+la_status la_decode_step(const void* q, const void* k, const void* v, void* o, float* S,
+                         float* z, int B, int H, int Dk, int Dv, la_dtype dt, float eps,
+                         la_stream_t stream) {
+    la_status s = check_common(B, H, 1, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if ((s = check_eps(eps)) != LA_OK) return s;
+    const int64_t BH = (int64_t)B * H;
+    if (BH == 0) return LA_OK;
+    if ((s = check_tensor(q, BH * Dk, dt)) || (s = check_tensor(k, BH * Dk, dt)) ||
+        (s = check_tensor(v, BH * Dv, dt)) || (s = check_tensor(o, BH * Dv, dt)))
+        return s;
+    if (!S || !z || !aligned(S, 16) || !aligned(z, 4)) return LA_ERR_INVALID_ARG;
+    return from_cuda(la::decode_step(q, k, v, o, S, z, dt, BH, Dk, Dv, eps, (cudaStream_t)stream));
+}
+
+la_status la_query_status(void* workspace, la_stream_t stream) {
+    if (!workspace || !aligned(workspace, 256)) return LA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t code = 0;
+    if (cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost, st))
+        return LA_ERR_CUDA;
+    if (cudaStreamSynchronize(st)) return LA_ERR_CUDA;
+    if (code != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st)) return LA_ERR_CUDA;
+        if (cudaStreamSynchronize(st)) return LA_ERR_CUDA;
+        return (la_status)code;
+    }
+    return LA_OK;
+}
+
+}  // extern "C"

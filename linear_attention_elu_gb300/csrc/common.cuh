@@ -1,0 +1,48 @@
+// Device-side helpers shared by the kernels of the linear-attention library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "linattn.h"
+
+namespace la {
+
+// Largest head dimension any path accepts (Dk and Dv).
+constexpr int kMaxDim = 128;
+// Tokens per chunk of the chunked causal evaluation.
+constexpr int kChunk = 64;
+
+// phi(x) = elu(x) + 1: x + 1 for x > 0, exp(x) otherwise ("Why Replace
+// Attention? The Softmax Bottleneck and the Path to Linear Time", section 5.3).
+__device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    uint32_t status;     // 0 = ok, else an la_status code set by a kernel
+    uint32_t epoch;      // launch generation for flag-based cross-CTA waits
+    uint32_t ticket;     // dynamic work-item counter of the running launch
+    uint32_t done;       // CTAs finished in the running launch
+    uint32_t max_spin;   // iteration limit of every bounded wait
+    uint32_t hold_item;  // test hook: work item + 1 whose publication is withheld
+    uint32_t pad[58];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr uint32_t kDefaultMaxSpin = 1u << 22;  // ~0.5 s with 100 ns backoff
+
+__device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
+    atomicCAS(&h->status, 0u, code);
+}
+
+}  // namespace la

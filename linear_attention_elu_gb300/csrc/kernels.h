@@ -1,0 +1,27 @@
+// Host-side launchers of the device kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "linattn.h"
+
+namespace la {
+
+// fp32-arithmetic SIMT paths (any 1 <= D, M <= 128, either dtype).
+size_t simt_causal_workspace(int64_t BH, int N, int D, int M);
+size_t simt_noncausal_workspace(int64_t BH, int N, int D, int M);
+int simt_noncausal_splits(int64_t BH, int N);
+cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
+                        int64_t BH, int N, int D, int M, float eps, float* S_out, float* z_out,
+                        void* scratch, cudaStream_t st);
+cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
+                           int64_t BH, int N, int D, int M, float eps, void* scratch,
+                           cudaStream_t st);
+
+// Decode step (SIMT, bandwidth bound).
+cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,
+                        la_dtype dt, int64_t BH, int D, int M, float eps, cudaStream_t st);
+
+}  // namespace la

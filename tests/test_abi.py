@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments synchronously (no GPU needed:
+every call here returns before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import linear_attention_elu_gb300 as la
+    return la
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(la_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_workspace_size",
+                     "la_workspace_init", "la_query_status", "la_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.library_path())
+    missing = [n for n in _declared() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.la_status_string(code).startswith("LA_")
+    assert "unknown" in lib.la_status_string(99)
+    assert lib.la_version() >= 1
+
+
+def test_workspace_size(lib):
+    assert lib.la_workspace_size(lib.LA_OP_DECODE, 512, 8, 1, 64, 64, lib.LA_BF16) == 0
+    for op in (lib.LA_OP_CAUSAL, lib.LA_OP_NONCAUSAL):
+        n = lib.la_workspace_size(op, 8, 8, 3072, 64, 64, lib.LA_BF16)
+        assert n >= 256 and n % 256 == 0
+        # Empty problems need only the header.
+        assert lib.la_workspace_size(op, 8, 8, 0, 64, 64, lib.LA_BF16) == 256
+
+
+def _raw(lib):
+    return ctypes.CDLL(lib.library_path())
+
+
+def test_bad_arguments_are_rejected_synchronously(lib):
+    so = _raw(lib)
+    n = ctypes.c_size_t(0)
+    # Null out-parameter, bad op, bad dtype, negative and oversized dims.
+    assert so.la_workspace_size(1, 1, 1, 1, 64, 64, 1, None) == 1
+    assert so.la_workspace_size(7, 1, 1, 1, 64, 64, 1, ctypes.byref(n)) == 1
+    assert so.la_workspace_size(1, 1, 1, 1, 64, 64, 5, ctypes.byref(n)) == 1
+    assert so.la_workspace_size(1, -1, 1, 1, 64, 64, 1, ctypes.byref(n)) == 1
+    assert so.la_workspace_size(1, 1, 1, 1, 0, 64, 1, ctypes.byref(n)) == 1
+    assert so.la_workspace_size(1, 1, 1, 1, 256, 256, 1, ctypes.byref(n)) == 2
+    assert so.la_workspace_size(1, 1000, 1000, 1, 64, 64, 1, ctypes.byref(n)) == 2
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    so.la_causal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P]
+    so.la_noncausal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, Z, P]
+    so.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+    fake = 1 << 20  # aligned, never dereferenced: every call below fails its checks first
+    # Null tensors.
+    assert so.la_causal_fwd(None, fake, fake, fake, 1, 1, 64, 64, 64, 1, 1e-6, None, None,
+                            fake, 1 << 30, None) == 1
+    # Misaligned tensor.
+    assert so.la_noncausal_fwd(fake + 2, fake, fake, fake, 1, 1, 64, 64, 64, 1, 1e-6, fake,
+                               1 << 30, None) == 1
+    # Negative / NaN eps.
+    assert so.la_causal_fwd(fake, fake, fake, fake, 1, 1, 64, 64, 64, 1, -1.0, None, None,
+                            fake, 1 << 30, None) == 1
+    assert so.la_causal_fwd(fake, fake, fake, fake, 1, 1, 64, 64, 64, 1, float("nan"), None,
+                            None, fake, 1 << 30, None) == 1
+    # Workspace missing, too small, misaligned.
+    assert so.la_causal_fwd(fake, fake, fake, fake, 1, 1, 64, 64, 64, 1, 1e-6, None, None,
+                            None, 0, None) == 3
+    assert so.la_causal_fwd(fake, fake, fake, fake, 1, 1, 64, 64, 64, 1, 1e-6, None, None,
+                            fake, 300, None) == 3
+    assert so.la_noncausal_fwd(fake, fake, fake, fake, 1, 1, 64, 64, 64, 1, 1e-6, fake + 16,
+                               1 << 30, None) == 3
+    # Decode: null state.
+    assert so.la_decode_step(fake, fake, fake, fake, None, fake, 1, 1, 64, 64, 1, 1e-6,
+                             None) == 1
+    # Empty problems are valid no-ops that touch nothing.
+    assert so.la_noncausal_fwd(None, None, None, None, 0, 4, 64, 64, 64, 1, 1e-6, None, 0,
+                               None) == 0
+    assert so.la_causal_fwd(None, None, None, None, 2, 0, 64, 64, 64, 1, 1e-6, None, None,
+                            None, 0, None) == 0
+    assert so.la_decode_step(None, None, None, None, None, None, 0, 8, 64, 64, 1, 1e-6,
+                             None) == 0

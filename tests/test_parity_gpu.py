@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Error measure (the pages give none; outputs are weighted means of N(0,1)
+values, so many entries sit near zero and element-wise relative error is
+ill-conditioned): for every output row (b, h, i),
+    max_d |gpu - oracle| / max_d |oracle|,
+and the gate is its maximum over rows: 1e-4 for float32 inputs, 2e-2 for
+bfloat16 inputs. The oracle sees the exact values the GPU sees (bf16/f32,
+upcast to float64).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, decode_token, make_qkv, make_workload, to_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_example_n4_d2.json")
+
+
+@pytest.fixture(scope="module")
+def la():
+    import linear_attention_elu_gb300 as m
+    return m
+
+
+def rowwise_rel(got, ref):
+    num = np.abs(got - ref).max(axis=-1)
+    den = np.maximum(np.abs(ref).max(axis=-1), 1e-30)
+    return float((num / den).max())
+
+
+def run(la, op, q, k, v, **kw):
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    fn = la.la_causal_fwd if op == "causal" else la.la_noncausal_fwd
+    o = fn(qd, kd, vd, **kw)
+    torch.cuda.synchronize()
+    return to_f64(o)
+
+
+def ref(op, q, k, v, eps=1e-6):
+    return oracle.recurrent(to_f64(q), to_f64(k), to_f64(v), causal=(op == "causal"), eps=eps)
+
+
+# ------------------------------------------------------------ worked example
+
+
+@pytest.mark.parametrize("op", ["causal", "noncausal"])
+def test_worked_example(la, op):
+    ex = json.load(open(GOLDEN))
+    q, k, v = (torch.tensor(ex[n], dtype=torch.float32).view(1, 1, 4, 2) for n in "QKV")
+    got = run(la, op, q, k, v, eps=0.0)[0, 0]
+    if op == "causal":
+        for step in ex["causal"]:
+            exact = np.array(step["o"]["num"], float) / step["o"]["den"]
+            np.testing.assert_allclose(got[step["i"] - 1], exact, rtol=1e-6, atol=1e-7)
+    else:
+        o1 = np.array(ex["noncausal"]["o1"]["num"], float) / ex["noncausal"]["o1"]["den"]
+        np.testing.assert_allclose(got[0], o1, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(got, ref(op, q, k, v, eps=0.0)[0, 0], rtol=1e-6, atol=1e-7)
+
+
+# ------------------------------------------------------------ small shapes
+
+
+@pytest.mark.parametrize("op", ["causal", "noncausal"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 63, 64, 65, 127, 200, 1000])
+def test_ragged_lengths(la, op, dtype, N):
+    q, k, v = make_qkv(2, 3, N, 64, dtype, seed=N)
+    err = rowwise_rel(run(la, op, q, k, v), ref(op, q, k, v))
+    assert err <= TOL[dtype], err
+
+
+@pytest.mark.parametrize("op", ["causal", "noncausal"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Dk,Dv", [(128, 128), (2, 2), (17, 33), (64, 32), (128, 64), (1, 1)])
+def test_head_dims(la, op, dtype, Dk, Dv):
+    q, k, _ = make_qkv(1, 2, 300, Dk, dtype, seed=Dk * 1000 + Dv)
+    _, _, v = make_qkv(1, 2, 300, Dv, dtype, seed=Dv)
+    err = rowwise_rel(run(la, op, q, k, v), ref(op, q, k, v))
+    assert err <= TOL[dtype], err
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_config(la, seed):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_workload(w, seed)
+    for op in ("causal", "noncausal"):
+        got = run(la, op, q, k, v)
+        r_quad = oracle.quadratic(to_f64(q), to_f64(k), to_f64(v), causal=(op == "causal"))
+        assert rowwise_rel(got, r_quad) <= TOL["f32"]
+        assert rowwise_rel(got, ref(op, q, k, v)) <= TOL["f32"]
+
+
+def test_causal_final_state(la):
+    q, k, v = make_qkv(2, 2, 333, 64, "f32", seed=3)
+    dev = torch.device("cuda")
+    S = torch.full((2, 2, 64, 64), float("nan"), device=dev)
+    z = torch.full((2, 2, 64), float("nan"), device=dev)
+    la.la_causal_fwd(q.to(dev), k.to(dev), v.to(dev), S_out=S, z_out=z)
+    torch.cuda.synchronize()
+    _, Sr, zr = oracle.recurrent(to_f64(q), to_f64(k), to_f64(v), True, return_state=True)
+    np.testing.assert_allclose(to_f64(S), Sr, rtol=1e-4, atol=1e-3)
+    np.testing.assert_allclose(to_f64(z), zr, rtol=1e-5, atol=1e-4)
+
+
+def test_empty_sequence(la):
+    dev = torch.device("cuda")
+    q = torch.empty(2, 3, 0, 64, device=dev)
+    S = torch.full((2, 3, 64, 64), 7.0, device=dev)
+    z = torch.full((2, 3, 64), 7.0, device=dev)
+    o = la.la_causal_fwd(q, q, q, S_out=S, z_out=z)
+    assert o.shape == (2, 3, 0, 64)
+    assert la.la_noncausal_fwd(q, q, q).shape == (2, 3, 0, 64)
+    torch.cuda.synchronize()
+    assert float(S.abs().max()) == 0.0 and float(z.abs().max()) == 0.0
+
+
+def test_degenerate_denominator(la):
+    # A query far in the negative range: phi(q) = exp(q) underflows, the
+    # denominator falls to eps and the row must stay finite and match the oracle.
+    q, k, v = make_qkv(1, 1, 100, 64, "f32", seed=4)
+    q[0, 0, 10] = -200.0
+    for op in ("causal", "noncausal"):
+        got = run(la, op, q, k, v)
+        assert np.all(np.isfinite(got))
+        r = ref(op, q, k, v)
+        # exp(-200) underflows to 0 in fp32 (num = 0, den = eps) but not in
+        # double (num ~ 1e-87, den ~ eps): both rows are 0 to within 1e-70.
+        assert np.abs(got[0, 0, 10]).max() <= 1e-70 and np.abs(r[0, 0, 10]).max() <= 1e-70
+        keep = np.ones(100, bool)
+        keep[10] = False
+        assert rowwise_rel(got[0, 0, keep], r[0, 0, keep]) <= TOL["f32"]
+
+
+def test_constant_phi_running_mean(la):
+    dev = torch.device("cuda")
+    N, D = 500, 64
+    z0 = torch.zeros(1, 1, N, D)
+    v = torch.randn(1, 1, N, D, generator=torch.Generator().manual_seed(0))
+    got = run(la, "causal", z0, z0, v, eps=0.0)[0, 0]
+    running = np.cumsum(to_f64(v)[0, 0], 0) / np.arange(1, N + 1)[:, None]
+    np.testing.assert_allclose(got, running, rtol=1e-4, atol=1e-5)
+    del dev
+
+
+def test_deterministic(la):
+    q, k, v = make_qkv(2, 4, 1000, 64, "bf16", seed=9)
+    a = run(la, "causal", q, k, v)
+    b = run(la, "causal", q, k, v)
+    np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------ full sizes
+
+
+def test_image_config_full(la):
+    w = WORKLOADS["image"]
+    q, k, v = make_workload(w, seed=0)
+    err = rowwise_rel(run(la, "causal", q, k, v), ref("causal", q, k, v))
+    assert err <= TOL[w.dtype], err
+
+
+def test_long_config_full(la):
+    w = WORKLOADS["long"]
+    q, k, v = make_workload(w, seed=0)
+    got = run(la, "causal", q, k, v)
+    err = rowwise_rel(got, ref("causal", q, k, v))
+    assert err <= TOL[w.dtype], err
+
+
+def test_bidir_config_sampled_heads(la):
+    w = WORKLOADS["bidir"]
+    q, k, v = make_workload(w, seed=0)
+    got = run(la, "noncausal", q, k, v)
+    B, H = w.B, w.H
+    rng = np.random.default_rng(0)
+    heads = rng.choice(B * H, size=6, replace=False)
+    qf, kf, vf = (to_f64(t).reshape(B * H, w.N, w.D) for t in (q, k, v))
+    r = oracle.recurrent(qf[heads], kf[heads], vf[heads], causal=False)
+    err = rowwise_rel(got.reshape(B * H, w.N, w.D)[heads], r)
+    assert err <= TOL[w.dtype], err
+
+
+# ------------------------------------------------------------ decode
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 64), ("f32", 64), ("f32", 2), ("bf16", 128)])
+def test_decode_steps(la, dtype, D):
+    dev = torch.device("cuda")
+    B, H = 16, 4
+    S = torch.zeros(B, H, D, D, device=dev)
+    z = torch.zeros(B, H, D, device=dev)
+    Sr, zr = np.zeros((B, H, D, D)), np.zeros((B, H, D))
+    for step in range(6):
+        q, k, v = decode_token(B, H, D, step, dtype, seed=1)
+        o = la.la_decode_step(q.to(dev), k.to(dev), v.to(dev), S, z)
+        r = oracle.decode_step(to_f64(q), to_f64(k), to_f64(v), Sr, zr)
+        torch.cuda.synchronize()
+        assert rowwise_rel(to_f64(o), r) <= TOL[dtype]
+    np.testing.assert_allclose(to_f64(S), Sr, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(to_f64(z), zr, rtol=1e-6, atol=1e-6)
+
+
+def test_decode_config_heads(la):
+    w = WORKLOADS["decode"]
+    dev = torch.device("cuda")
+    S = torch.zeros(w.B, w.H, w.D, w.D, device=dev)
+    z = torch.zeros(w.B, w.H, w.D, device=dev)
+    Sr, zr = np.zeros((w.B, w.H, w.D, w.D)), np.zeros((w.B, w.H, w.D))
+    for step in range(3):
+        q, k, v = decode_token(w.B, w.H, w.D, step, w.dtype, seed=0)
+        o = la.la_decode_step(q.to(dev), k.to(dev), v.to(dev), S, z)
+        r = oracle.decode_step(to_f64(q), to_f64(k), to_f64(v), Sr, zr)
+        torch.cuda.synchronize()
+        assert rowwise_rel(to_f64(o), r) <= TOL[w.dtype]
+
+
+def test_decode_sequence_equals_causal(la):
+    # N decode steps from the zero state reproduce the causal forward rows, and
+    # the causal forward's final state continues the sequence.
+    dev = torch.device("cuda")
+    B, H, N, D = 2, 4, 96, 64
+    q, k, v = make_qkv(B, H, N, D, "f32", seed=12)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    oc = la.la_causal_fwd(qd, kd, vd)
+    S = torch.zeros(B, H, D, D, device=dev)
+    z = torch.zeros(B, H, D, device=dev)
+    od = torch.stack([la.la_decode_step(qd[:, :, i].contiguous(), kd[:, :, i].contiguous(),
+                                        vd[:, :, i].contiguous(), S, z) for i in range(N)], 2)
+    torch.cuda.synchronize()
+    assert rowwise_rel(to_f64(od), to_f64(oc)) <= 1e-4
+    S2 = torch.empty_like(S)
+    z2 = torch.empty_like(z)
+    la.la_causal_fwd(qd, kd, vd, S_out=S2, z_out=z2)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_f64(S2), to_f64(S), rtol=1e-4, atol=1e-3)
+    np.testing.assert_allclose(to_f64(z2), to_f64(z), rtol=1e-5, atol=1e-4)
