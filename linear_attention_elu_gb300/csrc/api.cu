@@ -39,10 +39,10 @@ la_status check_eps(float eps) {
 
 size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
     const int64_t BH = (int64_t)B * H;
-    (void)dt;
     if (BH == 0 || N == 0) return 0;
     switch (op) {
         case LA_OP_CAUSAL:
+            if (la::tc_causal_supported(Dk, Dv, dt)) return la::tc_causal_workspace(BH, N);
             return la::simt_causal_workspace(BH, N, Dk, Dv);
         case LA_OP_NONCAUSAL:
             return la::simt_noncausal_workspace(BH, N, Dk, Dv);
@@ -113,7 +113,12 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
         *launches = 0;
         return LA_OK;
     }
-    *launches = op == LA_OP_DECODE ? 1 : 3;
+    if (op == LA_OP_DECODE)
+        *launches = 1;
+    else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
+        *launches = la::tc_causal_launches();
+    else
+        *launches = 3;
     return LA_OK;
 }
 
@@ -169,6 +174,8 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, in
     const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL, B, H, N, Dk, Dv, dt);
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
+    if (la::tc_causal_supported(Dk, Dv, dt))
+        return from_cuda(la::tc_causal(q, k, v, o, BH, N, eps, S_out, z_out, workspace, body, st));
     return from_cuda(
         la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, S_out, z_out, body, st));
 }

@@ -20,6 +20,14 @@ cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o,
                            int64_t BH, int N, int D, int M, float eps, void* scratch,
                            cudaStream_t st);
 
+// Tensor-core (tcgen05) causal path: bf16, Dk = Dv = 64.
+bool tc_causal_supported(int D, int M, la_dtype dt);
+size_t tc_causal_workspace(int64_t BH, int N);
+int tc_causal_launches();
+cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
+                      float eps, float* S_out, float* z_out, void* ws_header, void* scratch,
+                      cudaStream_t st);
+
 // Decode step (SIMT, bandwidth bound).
 cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,
                         la_dtype dt, int64_t BH, int D, int M, float eps, cudaStream_t st);

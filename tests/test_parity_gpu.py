@@ -244,3 +244,44 @@ def test_decode_sequence_equals_causal(la):
     torch.cuda.synchronize()
     np.testing.assert_allclose(to_f64(S2), to_f64(S), rtol=1e-4, atol=1e-3)
     np.testing.assert_allclose(to_f64(z2), to_f64(z), rtol=1e-5, atol=1e-4)
+
+
+# ------------------------------------------------------------ tensor-core causal path
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 1, 128), (1, 1, 129), (2, 3, 1000),
+                                   (1, 2, 20000), (3, 5, 777), (40, 8, 256), (1, 1, 4096)])
+def test_tc_causal_partitions(la, B, H, N):
+    # Grids smaller than the SM count, heads spread over many CTAs, ragged tails.
+    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=B * 100 + H * 10 + N)
+    err = rowwise_rel(run(la, "causal", q, k, v), ref("causal", q, k, v))
+    assert err <= TOL["bf16"], err
+
+
+def test_tc_causal_final_state(la):
+    B, H, N = 2, 3, 1500
+    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=21)
+    dev = torch.device("cuda")
+    S = torch.full((B, H, 64, 64), float("nan"), device=dev)
+    z = torch.full((B, H, 64), float("nan"), device=dev)
+    la.la_causal_fwd(q.to(dev), k.to(dev), v.to(dev), S_out=S, z_out=z)
+    torch.cuda.synchronize()
+    _, Sr, zr = oracle.recurrent(to_f64(q), to_f64(k), to_f64(v), True, return_state=True)
+    # S accumulates bf16-rounded phi(k) v products in fp32: compare per head in norm.
+    Sg = to_f64(S)
+    rel = np.abs(Sg - Sr).max(axis=(-1, -2)) / np.abs(Sr).max(axis=(-1, -2))
+    assert rel.max() <= 1e-2, rel.max()
+    np.testing.assert_allclose(to_f64(z), zr, rtol=5e-3)
+
+
+def test_tc_causal_long_config_rows_sampled_against_quadratic(la):
+    # Full-size long-context run checked row by row against the quadratic definition.
+    w = WORKLOADS["long"]
+    q, k, v = make_workload(w, seed=1)
+    got = run(la, "causal", q, k, v).reshape(w.B * w.H, w.N, w.D)
+    rng = np.random.default_rng(1)
+    heads = rng.integers(0, w.B * w.H, 24)
+    idx = np.concatenate([[0, 127, 128, w.N - 1], rng.integers(0, w.N, 20)])
+    qf, kf, vf = (to_f64(t).reshape(w.B * w.H, w.N, w.D) for t in (q, k, v))
+    r = oracle.rows(qf, kf, vf, True, heads, idx)
+    assert rowwise_rel(got[heads, idx], r) <= TOL[w.dtype]
