@@ -25,7 +25,7 @@ __all__ = [
 
 LA_F32, LA_BF16 = 0, 1
 LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE = 0, 1, 2
-LA_OK, LA_ERR_TIMEOUT = 0, 5
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 
 _DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
 
