@@ -119,6 +119,32 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
                         void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * Causal forward for callers that cannot allocate device memory: a plugin
+ * host that passes only input and output buffers, a real-time process that
+ * forbids device allocation once it runs, or code whose memory belongs to
+ * another framework's allocator. The paper has no counterpart; this is a
+ * property of the library. It computes exactly what la_causal_fwd computes
+ * (same arguments, minus the workspace) and allocates nothing: its scratch is
+ * one fixed 16 MiB array in device memory that belongs to this library, held
+ * by every GPU that loads it until the process exits.
+ *  - The first call on a device looks up that array's device address and
+ *    initialises its header on `stream`; make that first call before any
+ *    stream capture.
+ *  - Shapes whose scratch would exceed 16 MiB return LA_ERR_WORKSPACE and
+ *    launch nothing. For bf16 with Dk = Dv = 64 on a 152-SM GPU every shape
+ *    with B*H <= 760 fits, whatever N; the fp32 path keeps one state per
+ *    64-token chunk and fits B*H*ceil(N/64) <= 1008 at Dk = Dv = 64.
+ *  - All calls share the one array, which keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams, or concurrent host
+ *    threads without ordering) race on it and must be serialised by the caller.
+ *  - Device-side wait timeouts are recorded in the array's header, which the
+ *    caller cannot query.
+ */
+la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                                int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                                float* S_out, float* z_out, la_stream_t stream);
+
+/*
  * One recurrent decode step for B*H independent heads, in place:
  * S <- S + phi(k) v^T, z <- z + phi(k), o = phi(q)^T S / (phi(q)^T z + eps).
  * q, k: [B,H,Dk]; v, o: [B,H,Dv] in dtype dt; S: [B,H,Dk,Dv] and z: [B,H,Dk]
