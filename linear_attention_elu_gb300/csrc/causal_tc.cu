@@ -319,28 +319,46 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // ======================================================== output kernel
-// Warps 0-7: phi pass and epilogues (two warpgroups; warpgroup g takes half of
-// the columns of every TMEM read). Warp 8: TMA producer. Warp 9: MMA issuer.
+// Warp roles (14 warps):
+//   warps 0-3   phi:   phi on the Q and K tiles of each landed stage, in place
+//   warps 4-7   mask:  A -> causal mask -> bf16 P (shared memory), per chunk
+//   warps 8-11  state: [dS | dz] -> running state -> next snapshot; then the
+//                      output epilogue num / (den + eps) -> TMA store
+//   warp 12     TMA producer       warp 13  MMA issuer (one thread)
+// The four warps of a role cover the four TMEM lane quarters.
 
-constexpr int kOutThreads = 320;
-constexpr int kMath = 256;
+constexpr int kOutThreads = 448;
+constexpr int kStages = 3;
 // Shared-memory map (offsets from a 1024-aligned base).
-constexpr uint32_t kStageBytes = 3 * kTileBytes;           // Q, K, V tiles
-constexpr uint32_t kOffP = 2 * kStageBytes;                // masked A, bf16, 2 sub-tiles
-constexpr uint32_t kOffSnap = kOffP + 2 * kTileBytes;      // 2 x [S | z] snapshot
-constexpr uint32_t kSnapAtom = kD * 128;                   // 64 rows x 128 B
-constexpr uint32_t kOffOnes = kOffSnap + 4 * kSnapAtom;    // ones tile (128 x 64)
-constexpr uint32_t kOffO = kOffOnes + kTileBytes;          // 2 x output staging tile
-constexpr uint32_t kSmemEnd = kOffO + 2 * kTileBytes;
+constexpr uint32_t kStageBytes = 3 * kTileBytes;               // Q, K, V tiles
+constexpr uint32_t kOffP = kStages * kStageBytes;              // masked A, bf16, 2 sub-tiles
+constexpr uint32_t kSnapS = kD * 128;                          // S snapshot: 64 rows x 128 B
+constexpr uint32_t kSnapZ = 16 * 128;                          // z tile: 16 rows x 128 B (K-major)
+constexpr uint32_t kSnapBytes = kSnapS + kSnapZ;
+constexpr uint32_t kOffSnap = kOffP + 2 * kTileBytes;          // 2 x (S | z)
+constexpr uint32_t kOffOnes = kOffSnap + 2 * kSnapBytes;       // ones: 16 rows x 128 keys, K-major
+constexpr uint32_t kOnesBytes = 2 * 16 * 128;
+constexpr uint32_t kOffO = kOffOnes + kOnesBytes;              // output staging tile
+constexpr uint32_t kSmemEnd = kOffO + kTileBytes;
 constexpr size_t kOutSmem = 1024 + kSmemEnd;
-// TMEM columns: A [0,128), dS [128,208), O[b] at 256 + 128 b (80 columns each).
-constexpr uint32_t kTmA = 0, kTmS = 128, kTmO = 256;
+// TMEM columns: A[b] at 128 b; O[b] = [num 64 | den 16] at 256 + 96 b; dS = [dS 64 | dz 16] at 432.
+constexpr uint32_t kTmO = 256, kTmOStride = 96, kTmS = 432;
 
 struct OutMisc {
-    uint64_t full[2], empty[2], phi_ready[2], mma1_done[2], s_ready[2], p_ready[2],
-        mma2_done[2], o_free[2], mma_drain;
+    uint64_t full[kStages], phi_done[kStages], empty[kStages];
+    uint64_t a_full[2], a_free[2], o_full[2], o_free[2], snap_full[2];
+    uint64_t p_full, p_free, ds_full, ds_free, state_init, mma_drain;
     uint32_t tmem_slot;
 };
+
+// K-major "ones" operand: row 0 = 1.0 over 128 keys (two 64-key sub-tiles), rows 1-15 = 0.
+__device__ __forceinline__ void init_ones_kmajor(uint8_t* t, int tid, int nthreads) {
+    for (int idx = tid; idx < 2 * 16 * 8; idx += nthreads) {
+        const int sub = idx / 128, r = (idx / 8) % 16, pc = idx % 8;
+        const uint32_t one = r == 0 ? 0x3F803F80u : 0u;
+        *reinterpret_cast<uint4*>(t + sub * 2048 + r * 128 + pc * 16) = make_uint4(one, one, one, one);
+    }
+}
 
 __global__ void __launch_bounds__(kOutThreads, 1)
 causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -362,37 +380,45 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
     auto stage_k = [&](int s) { return base + s * kStageBytes + kTileBytes; };
     auto stage_v = [&](int s) { return base + s * kStageBytes + 2 * kTileBytes; };
     uint8_t* sP = base + kOffP;
-    auto snap = [&](int b) { return base + kOffSnap + 2 * b * kSnapAtom; };
+    auto snap_s = [&](int b) { return base + kOffSnap + b * kSnapBytes; };
+    auto snap_z = [&](int b) { return base + kOffSnap + b * kSnapBytes + kSnapS; };
     uint8_t* ones = base + kOffOnes;
-    auto ostage = [&](int b) { return base + kOffO + b * kTileBytes; };
+    uint8_t* ostage = base + kOffO;
 
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&m.full[b], 1);
-            mbar_init(&m.empty[b], 1);
-            mbar_init(&m.phi_ready[b], 1);
-            mbar_init(&m.mma1_done[b], 1);
-            mbar_init(&m.s_ready[b], 1);
-            mbar_init(&m.p_ready[b], 1);
-            mbar_init(&m.mma2_done[b], 1);
-            mbar_init(&m.o_free[b], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&m.full[s], 1);
+            mbar_init(&m.phi_done[s], 1);
+            mbar_init(&m.empty[s], 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&m.a_full[b], 1);
+            mbar_init(&m.a_free[b], 1);
+            mbar_init(&m.o_full[b], 1);
+            mbar_init(&m.o_free[b], 1);
+            mbar_init(&m.snap_full[b], 1);
+        }
+        mbar_init(&m.p_full, 1);
+        mbar_init(&m.p_free, 1);
+        mbar_init(&m.ds_full, 1);
+        mbar_init(&m.ds_free, 1);
+        mbar_init(&m.state_init, 1);
         mbar_init(&m.mma_drain, 1);
         fence_mbar_init();
     }
-    if (warp < 8) {
-        init_ones_tile(ones, tid, kMath);
-        // z atoms of both snapshots: only logical columns 0, 1 are ever rewritten.
-        for (int idx = tid; idx < 2 * kSnapAtom / 16; idx += kMath) {
-            const int b = idx / (kSnapAtom / 16), r = idx % (kSnapAtom / 16);
-            *reinterpret_cast<uint4*>(snap(b) + kSnapAtom + r * 16) = make_uint4(0, 0, 0, 0);
+    if (warp < 12) {
+        init_ones_kmajor(ones, tid, 384);
+        for (int idx = tid; idx < 2 * (int)kSnapZ / 16; idx += 384) {  // both z tiles
+            const int b = idx / (kSnapZ / 16), r = idx % (kSnapZ / 16);
+            *reinterpret_cast<uint4*>(snap_z(b) + r * 16) = make_uint4(0, 0, 0, 0);
         }
     }
-    if (warp == 9) {
+    fence_proxy_async_smem();
+    if (warp == 13) {
         tmem_alloc(&m.tmem_slot, 512);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
@@ -402,14 +428,17 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = m.tmem_slot;
+    const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             int i = 0;
             for (; i < nch; ++i) {
-                const int s = i & 1;
-                if (i >= 2 && !mbar_wait(&m.empty[s], ((i >> 1) - 1) & 1, max_spin)) {
+                const int s = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(&m.empty[s], ((i / kStages) - 1) & 1, max_spin)) {
                     report_timeout(hdr);
                     break;
                 }
@@ -421,266 +450,366 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
                 tma_load_3d(stage_k(s), &kmap, &m.full[s], 0, ch * kC, h);
                 tma_load_3d(stage_v(s), &vmap, &m.full[s], 0, ch * kC, h);
             }
-            for (int j = i - 2 > 0 ? i - 2 : 0; j < i; ++j)
-                mbar_wait(&m.full[j & 1], (j >> 1) & 1, kDefaultMaxSpin);
+            for (int j = i - kStages > 0 ? i - kStages : 0; j < i; ++j)
+                mbar_wait(&m.full[j % kStages], (j / kStages) & 1, kDefaultMaxSpin);
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t id_kv = idesc_bf16_f32(64, kNx, true, true);
-            const uint32_t id_o = idesc_bf16_f32(128, kNx, false, true);
-            const uint32_t onesa = smem_u32(ones);
+            const uint32_t id_kv = idesc_bf16_f32(64, 64, true, true);
+            const uint32_t id_k1 = idesc_bf16_f32(64, 16, true, false);
+            const uint32_t id_o = idesc_bf16_f32(128, 64, false, true);
+            const uint32_t id_o1 = idesc_bf16_f32(128, 16, false, false);
+            const uint32_t onesa = smem_u32(ones), pa = smem_u32(sP);
+            const uint32_t tS = tmem + kTmS;
             for (int i = 0; i < nch; ++i) {
-                const int b = i & 1;
-                const uint32_t par = (i >> 1) & 1;
-                const uint32_t tO = tmem + kTmO + 128u * b;
-                if (!mbar_wait(&m.phi_ready[b], par, max_spin)) { report_timeout(hdr); break; }
+                const int s = i % kStages, b = i & 1;
+                const uint32_t pb = (i >> 1) & 1, pi = i & 1;
+                const uint32_t tA = tmem + 128u * b, tO = tmem + kTmO + kTmOStride * b;
+                if (!mbar_wait(&m.phi_done[s], (i / kStages) & 1, max_spin)) { report_timeout(hdr); break; }
+                if (i >= 2 && !mbar_wait(&m.a_free[b], pb ^ 1, max_spin)) { report_timeout(hdr); break; }
                 tc_fence_after();
-                const uint32_t qa = smem_u32(stage_q(b)), ka = smem_u32(stage_k(b)),
-                               va = smem_u32(stage_v(b));
-                const uint32_t lbo_v1 = onesa - va;  // [V | 1]
+                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
+                               va = smem_u32(stage_v(s));
                 // (1) A = phi(Q) phi(K)^T: M=128 queries, N=128 keys, K=64 features.
 #pragma unroll
                 for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tmem + kTmA, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
+                    mma_bf16(tA, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
                              smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_qk, k16 > 0);
-                // (2) [dS | dz] = phi(K)^T [V | 1]: M=64 features, N=80, K=128 tokens.
-#pragma unroll
-                for (int k16 = 0; k16 < kC / 16; ++k16)
-                    mma_bf16(tmem + kTmS, smem_desc(ka + k16 * 2048, 1024, 1024, kSwizzle128B),
-                             smem_desc(va + k16 * 2048, lbo_v1, 1024, kSwizzle128B), id_kv,
-                             k16 > 0);
-                mma_commit(&m.mma1_done[b]);
-                // (3) [num | den] = phi(Q) [S_prev | z_hi z_lo]: needs the snapshot and a free O.
-                if (i >= 2 && !mbar_wait(&m.o_free[b], par ^ 1, max_spin)) {
-                    report_timeout(hdr);
-                    break;
-                }
-                if (!mbar_wait(&m.s_ready[b], par, max_spin)) { report_timeout(hdr); break; }
+                mma_commit(&m.a_full[b]);
+                // (2) S += phi(K)^T V (M=64, N=64) and (2b) z += phi(K)^T 1 (N=16), K=128
+                // tokens: the running state [S | z] of the current run lives in TMEM. The
+                // first run starts from the state written by the state role; a later run
+                // starts a new head from zero.
+                const int64_t u = u0 + i;
+                const bool run_start = (u % part.nchunks == 0);
+                if (i == 0 && !mbar_wait(&m.state_init, 0, max_spin)) { report_timeout(hdr); break; }
+                if (i >= 1 && !mbar_wait(&m.ds_free, pi ^ 1, max_spin)) { report_timeout(hdr); break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(snap(b));
+                const bool fresh = (i > 0 && run_start);
 #pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tO, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(sa + k16 * 2048, kSnapAtom, 1024, kSwizzle128B), id_o,
-                             k16 > 0);
-                // (4) [num | den] += P [V | 1]: K = 128 keys (P in two 64-key sub-tiles).
-                if (!mbar_wait(&m.p_ready[b], par, max_spin)) { report_timeout(hdr); break; }
-                tc_fence_after();
-                const uint32_t pa = smem_u32(sP);
-#pragma unroll
-                for (int k16 = 0; k16 < kC / 16; ++k16)
-                    mma_bf16(tO,
-                             smem_desc(pa + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16, 1024,
+                for (int k16 = 0; k16 < kC / 16; ++k16) {
+                    const uint64_t kd = smem_desc(ka + k16 * 2048, 1024, 1024, kSwizzle128B);
+                    const uint32_t acc = (fresh && k16 == 0) ? 0u : 1u;
+                    mma_bf16(tS, kd, smem_desc(va + k16 * 2048, 1024, 1024, kSwizzle128B), id_kv,
+                             acc);
+                    mma_bf16(tS + 64, kd,
+                             smem_desc(onesa + (k16 >> 2) * 2048 + (k16 & 3) * 32, 16, 1024,
                                        kSwizzle128B),
-                             smem_desc(va + k16 * 2048, lbo_v1, 1024, kSwizzle128B), id_o, 1u);
-                mma_commit(&m.mma2_done[b]);
-                mma_commit(&m.empty[b]);
+                             id_k1, acc);
+                }
+                mma_commit(&m.ds_full);
+                // (3) num = phi(Q) S_prev and (3b) den = phi(Q) [z_hi; z_lo]: needs the snapshot, free O.
+                if (!mbar_wait(&m.snap_full[b], pb, max_spin)) { report_timeout(hdr); break; }
+                if (i >= 2 && !mbar_wait(&m.o_free[b], pb ^ 1, max_spin)) { report_timeout(hdr); break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(snap_s(b)), za = smem_u32(snap_z(b));
+#pragma unroll
+                for (int k16 = 0; k16 < kD / 16; ++k16) {
+                    const uint64_t qd = smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B);
+                    mma_bf16(tO, qd, smem_desc(sa + k16 * 2048, 1024, 1024, kSwizzle128B), id_o,
+                             k16 > 0);
+                    mma_bf16(tO + 64, qd, smem_desc(za + k16 * 32, 16, 1024, kSwizzle128B), id_o1,
+                             k16 > 0);
+                }
+                // (4) num += P V and (4b) den += P 1: K = 128 keys (P in two 64-key sub-tiles).
+                if (!mbar_wait(&m.p_full, pi, max_spin)) { report_timeout(hdr); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < kC / 16; ++k16) {
+                    const uint64_t pd = smem_desc(pa + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16,
+                                                  1024, kSwizzle128B);
+                    mma_bf16(tO, pd, smem_desc(va + k16 * 2048, 1024, 1024, kSwizzle128B), id_o, 1u);
+                    mma_bf16(tO + 64, pd,
+                             smem_desc(onesa + (k16 >> 2) * 2048 + (k16 & 3) * 32, 16, 1024,
+                                       kSwizzle128B),
+                             id_o1, 1u);
+                }
+                mma_commit(&m.o_full[b]);
+                mma_commit(&m.p_free);
+                mma_commit(&m.empty[s]);
             }
             mma_commit(&m.mma_drain);  // every issued MMA completes before TMEM is released
             mbar_wait(&m.mma_drain, 0, kDefaultMaxSpin);
         }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- phi role
+        const int t = tid;  // 0..127
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
+            const int s = i % kStages;
+            const int ch = (int)((u0 + i) % part.nchunks);
+            const int valid = min(kC, N - ch * kC);
+            ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
+            uint8_t* qt = stage_q(s);
+            uint8_t* kt = stage_k(s);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 vq[4], vk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (t >> 3) + 16 * (4 * half + k);
+                    vq[k] = *reinterpret_cast<const uint4*>(qt + r * 128 + (t & 7) * 16);
+                    vk[k] = *reinterpret_cast<const uint4*>(kt + r * 128 + (t & 7) * 16);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (t >> 3) + 16 * (4 * half + k);
+                    *reinterpret_cast<uint4*>(qt + r * 128 + (t & 7) * 16) = phi8(vq[k]);
+                    *reinterpret_cast<uint4*>(kt + r * 128 + (t & 7) * 16) =
+                        r < valid ? phi8(vk[k]) : make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            ok = named_bar_and(1, 128, ok);
+            if (!ok) break;
+            if (t == 0) mbar_arrive(&m.phi_done[s]);
+        }
+        if (!ok && t == 0) report_timeout(hdr);
+    } else if (warp < 8) {
+        // ---------------------------------------------------------- mask role
+        const int row = 32 * q4 + lane;  // query row
+        const int t = tid - 128;
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1;
+            const uint32_t pb = (i >> 1) & 1;
+            const uint32_t tA = tmem + 128u * b;
+            ok = mbar_wait(&m.a_full[b], pb, max_spin);
+            if (i >= 1) ok = mbar_wait(&m.p_free, (i - 1) & 1, max_spin) && ok;
+            tc_fence_after();
+            // Key block j (32 keys): j < q4 fully visible, j == q4 holds the diagonal, j > q4 masked.
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint8_t* pt = sP + (j >> 1) * kTileBytes;
+                const int col0 = 32 * (j & 1);
+                if (j > q4) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(pt + sw128_offset(row, col0 + 8 * c)) =
+                            make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tA + lane_base + 32 * j, r0);
+                tmem_ld16(tA + lane_base + 32 * j + 16, r1);
+                tmem_ld_wait();
+                float a[32];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    a[e] = __uint_as_float(r0[e]);
+                    a[16 + e] = __uint_as_float(r1[e]);
+                }
+                if (j == q4) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a[e] = (e <= lane) ? a[e] : 0.f;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 v = make_uint4(pack_bf16(a[8 * c], a[8 * c + 1]),
+                                         pack_bf16(a[8 * c + 2], a[8 * c + 3]),
+                                         pack_bf16(a[8 * c + 4], a[8 * c + 5]),
+                                         pack_bf16(a[8 * c + 6], a[8 * c + 7]));
+                    *reinterpret_cast<uint4*>(pt + sw128_offset(row, col0 + 8 * c)) = v;
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            ok = named_bar_and(2, 128, ok);
+            if (!ok) break;
+            if (t == 0) {
+                mbar_arrive(&m.a_free[b]);
+                mbar_arrive(&m.p_full);
+            }
+        }
+        if (!ok && t == 0) report_timeout(hdr);
     } else {
-        // ---------------------------------------------------------- math warps
-        // Order per chunk i: (b)_i, then (a)_{i+1} (overlaps MMAs (3),(4) of i), then (c)_i.
-        // Every abort decision is ANDed over the 256 math threads at a barrier.
-        const int t = tid;
-        const int g = warp >> 2;                 // warpgroup: column half
-        const int q4 = warp & 3;                 // TMEM lane quarter
-        const int row = 32 * q4 + lane;          // query row (M = 128 layouts)
-        const int srow = 16 * q4 + (lane & 15);  // state row (M = 64 layout), lanes < 16
+        // ---------------------------------------------------------- state + output role
+        // The running state [S | z] is accumulated in TMEM by the MMAs (2), (2b)
+        // (M = 64 layout: state row r in lane 32 (r / 16) + r % 16). This role
+        // writes the first run's start state, reads the state after every chunk
+        // into the bf16 snapshot used by the next chunk's MMA (3), and writes the
+        // outputs.
+        const int t = tid - 256;                    // 0..127
+        const int row = 32 * q4 + lane;             // query row (M = 128 layout)
+        const int srow = 16 * q4 + (lane & 15);     // state row (M = 64 layout), lanes < 16
         const bool sowner = lane < 16;
-        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        float S_run[32];                         // state row srow, columns [32g, 32g + 32)
-        float z_run = 0.f;                       // z[srow] (warpgroup 0 owners)
+        const uint32_t tS = tmem + kTmS + lane_base;
 
         // Start state of the first run: sum of the aggregates of this head's
-        // chunks held by lower-numbered CTAs (written by the state kernel).
-        auto load_prefix = [&](int64_t u_first) {
-            const int h = (int)(u_first / part.nchunks);
-            const int64_t head_begin = (int64_t)h * part.nchunks;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) S_run[e] = 0.f;
-            z_run = 0.f;
-            if (u_first <= head_begin || !sowner) return;
-            for (int c2 = cta - 1; c2 >= 0; --c2) {
-                const int64_t b0 = part.begin(c2), b1 = part.begin(c2 + 1);
-                if (b1 <= head_begin) break;
-                if (b1 <= b0) continue;
-                const int r = (int)(h - b0 / part.nchunks);
-                const float* a = agg + ((int64_t)c2 * part.maxr + r) * kE;
-                const float4* src = reinterpret_cast<const float4*>(a + srow * kD + 32 * g);
-#pragma unroll
-                for (int qd = 0; qd < 8; ++qd) {
-                    float4 v = src[qd];
-                    S_run[4 * qd] += v.x;
-                    S_run[4 * qd + 1] += v.y;
-                    S_run[4 * qd + 2] += v.z;
-                    S_run[4 * qd + 3] += v.w;
-                }
-                z_run += a[kD * kD + srow];
-            }
-        };
-        // Snapshot b = bf16(S_run) (MN-major, row = feature) and z = z_hi + z_lo.
-        auto write_snap = [&](int b) {
-            if (!sowner) return;
-            uint8_t* d = snap(b);
-#pragma unroll
-            for (int cq = 0; cq < 4; ++cq) {
-                const int col = 32 * g + 8 * cq;
-                uint4 v = make_uint4(pack_bf16(S_run[8 * cq], S_run[8 * cq + 1]),
-                                     pack_bf16(S_run[8 * cq + 2], S_run[8 * cq + 3]),
-                                     pack_bf16(S_run[8 * cq + 4], S_run[8 * cq + 5]),
-                                     pack_bf16(S_run[8 * cq + 6], S_run[8 * cq + 7]));
-                *reinterpret_cast<uint4*>(d + sw128_offset(srow, col)) = v;
-            }
-            if (g == 0) {
-                const uint32_t hi = pack_bf16(z_run, 0.f);
-                const float zlo = z_run - bf_lo(hi);
-                *reinterpret_cast<uint32_t*>(d + kSnapAtom + sw128_offset(srow, 0)) =
-                    pack_bf16(bf_lo(hi), zlo);
-            }
-        };
-        // (a) phi on Q and K of chunk i in place (K rows past N set to 0).
-        auto phase_a = [&](int i) -> bool {
-            const int b = i & 1;
-            const int ch = (int)((u0 + i) % part.nchunks);
-            bool ok = mbar_wait(&m.full[b], (i >> 1) & 1, max_spin);
-            phi_tile_256(stage_q(b), t, kC);
-            phi_tile_256(stage_k(b), t, min(kC, N - ch * kC));
-            fence_proxy_async_smem();
-            ok = named_bar_and(1, kMath, ok);
-            if (ok && t == 0) mbar_arrive(&m.phi_ready[b]);
-            return ok;
-        };
-
+        // chunks held by lower-numbered CTAs (written by the state kernel), into
+        // TMEM and into snapshot 0.
         pdl_wait();  // the state kernel's aggregates are complete and visible
-        load_prefix(u0);
-        write_snap(0);
-        fence_proxy_async_smem();
-        named_bar(1, kMath);
-        if (t == 0) mbar_arrive(&m.s_ready[0]);
-        bool ok = phase_a(0);
-        for (int i = 0; i < nch && ok; ++i) {
+        {
+            const int h = (int)(u0 / part.nchunks);
+            const int64_t head_begin = (int64_t)h * part.nchunks;
+            float S0[kD];
+            float z0 = 0.f;
+#pragma unroll
+            for (int e = 0; e < kD; ++e) S0[e] = 0.f;
+            if (u0 > head_begin && sowner) {
+                for (int c2 = cta - 1; c2 >= 0; --c2) {
+                    const int64_t b0 = part.begin(c2), b1 = part.begin(c2 + 1);
+                    if (b1 <= head_begin) break;
+                    if (b1 <= b0) continue;
+                    const int r = (int)(h - b0 / part.nchunks);
+                    const float* a = agg + ((int64_t)c2 * part.maxr + r) * kE;
+                    const float4* src = reinterpret_cast<const float4*>(a + srow * kD);
+#pragma unroll
+                    for (int qd = 0; qd < kD / 4; ++qd) {
+                        float4 v = src[qd];
+                        S0[4 * qd] += v.x;
+                        S0[4 * qd + 1] += v.y;
+                        S0[4 * qd + 2] += v.z;
+                        S0[4 * qd + 3] += v.w;
+                    }
+                    z0 += a[kD * kD + srow];
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(S0[16 * c + e]);
+                tmem_st16(tS + 16 * c, w);
+            }
+            {
+                uint32_t w[16];
+                w[0] = __float_as_uint(z0);
+#pragma unroll
+                for (int e = 1; e < 16; ++e) w[e] = 0u;
+                tmem_st16(tS + 64, w);
+            }
+            tmem_st_wait();
+            if (sowner) {
+                uint8_t* d = snap_s(0);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = make_uint4(pack_bf16(S0[8 * c], S0[8 * c + 1]),
+                                         pack_bf16(S0[8 * c + 2], S0[8 * c + 3]),
+                                         pack_bf16(S0[8 * c + 4], S0[8 * c + 5]),
+                                         pack_bf16(S0[8 * c + 6], S0[8 * c + 7]));
+                    *reinterpret_cast<uint4*>(d + sw128_offset(srow, 8 * c)) = v;
+                }
+                const uint32_t hi = pack_bf16(z0, 0.f);
+                const uint32_t lo = pack_bf16(z0 - bf_lo(hi), 0.f);
+                *reinterpret_cast<uint16_t*>(snap_z(0) + sw128_offset(0, srow)) = (uint16_t)hi;
+                *reinterpret_cast<uint16_t*>(snap_z(0) + sw128_offset(1, srow)) = (uint16_t)lo;
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(3, 128);
+            if (t == 0) {
+                mbar_arrive(&m.state_init);
+                mbar_arrive(&m.snap_full[0]);
+            }
+        }
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
             const int b = i & 1;
-            const uint32_t par = (i >> 1) & 1;
+            const uint32_t pb = (i >> 1) & 1;
             const int64_t u = u0 + i;
             const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
             const bool last_in_run = (u + 1 == u1) || ((u + 1) / part.nchunks != h);
-            const uint32_t tO = tmem + kTmO + 128u * b;
+            const bool head_end = (ch == part.nchunks - 1);
 
-            // (b) masked A -> P (bf16); [dS | dz] -> running state -> next snapshot.
-            ok = mbar_wait(&m.mma1_done[b], par, max_spin);
+            // State after chunk i -> snapshot for chunk i + 1 (zero when a new head starts).
+            ok = mbar_wait(&m.ds_full, i & 1, max_spin);
             tc_fence_after();
-            {
-                uint8_t* pt = sP + g * kTileBytes;  // keys [64g, 64g + 64)
-                if (g == 1 && q4 < 2) {
-                    // Queries 0..63 see no key in 64..127.
+            const bool snap_next = (i + 1 < nch);
+            uint8_t* dnext = snap_s(b ^ 1);
 #pragma unroll
-                    for (int cq = 0; cq < 8; ++cq)
-                        *reinterpret_cast<uint4*>(pt + sw128_offset(row, 8 * cq)) =
-                            make_uint4(0, 0, 0, 0);
-                } else {
-                    const bool diag = (g == 0) == (q4 < 2);  // block holding the diagonal
-                    uint32_t r[4][16];
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tS + 32 * c2, r0);
+                tmem_ld16(tS + 32 * c2 + 16, r1);
+                tmem_ld_wait();
+                if (sowner && last_in_run && head_end && S_out) {
+                    float4* dst = reinterpret_cast<float4*>(S_out + ((int64_t)h * kD + srow) * kD + 32 * c2);
 #pragma unroll
-                    for (int cb = 0; cb < 4; ++cb)
-                        tmem_ld16(tmem + kTmA + lane_base + 64 * g + 16 * cb, r[cb]);
-                    tmem_ld_wait();
+                    for (int qd = 0; qd < 4; ++qd) {
+                        dst[qd] = make_float4(__uint_as_float(r0[4 * qd]), __uint_as_float(r0[4 * qd + 1]),
+                                              __uint_as_float(r0[4 * qd + 2]), __uint_as_float(r0[4 * qd + 3]));
+                        dst[qd + 4] = make_float4(__uint_as_float(r1[4 * qd]), __uint_as_float(r1[4 * qd + 1]),
+                                                  __uint_as_float(r1[4 * qd + 2]), __uint_as_float(r1[4 * qd + 3]));
+                    }
+                }
+                if (sowner && snap_next) {
 #pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
-                        float a[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int key = 64 * g + 16 * cb + e;
-                            a[e] = (!diag || key <= row) ? __uint_as_float(r[cb][e]) : 0.f;
-                        }
-#pragma unroll
-                        for (int hq = 0; hq < 2; ++hq) {
-                            uint4 v = make_uint4(pack_bf16(a[8 * hq], a[8 * hq + 1]),
-                                                 pack_bf16(a[8 * hq + 2], a[8 * hq + 3]),
-                                                 pack_bf16(a[8 * hq + 4], a[8 * hq + 5]),
-                                                 pack_bf16(a[8 * hq + 6], a[8 * hq + 7]));
-                            *reinterpret_cast<uint4*>(pt + sw128_offset(row, 16 * cb + 8 * hq)) = v;
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* rr = c < 2 ? r0 : r1;
+                        const int e0 = 8 * (c & 1);
+                        uint4 v = last_in_run
+                                      ? make_uint4(0, 0, 0, 0)
+                                      : make_uint4(pack_bf16(__uint_as_float(rr[e0]), __uint_as_float(rr[e0 + 1])),
+                                                   pack_bf16(__uint_as_float(rr[e0 + 2]), __uint_as_float(rr[e0 + 3])),
+                                                   pack_bf16(__uint_as_float(rr[e0 + 4]), __uint_as_float(rr[e0 + 5])),
+                                                   pack_bf16(__uint_as_float(rr[e0 + 6]), __uint_as_float(rr[e0 + 7])));
+                        *reinterpret_cast<uint4*>(dnext + sw128_offset(srow, 32 * c2 + 8 * c)) = v;
                     }
                 }
             }
             {
-                uint32_t r0[16], r1[16], rz[16];
-                tmem_ld16(tmem + kTmS + lane_base + 32 * g, r0);
-                tmem_ld16(tmem + kTmS + lane_base + 32 * g + 16, r1);
-                tmem_ld16(tmem + kTmS + lane_base + 64, rz);
+                uint32_t rz[16];
+                tmem_ld16(tS + 64, rz);
                 tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    S_run[e] += __uint_as_float(r0[e]);
-                    S_run[16 + e] += __uint_as_float(r1[e]);
+                const float zr = __uint_as_float(rz[0]);
+                if (sowner && last_in_run && head_end && z_out) z_out[(int64_t)h * kD + srow] = zr;
+                if (sowner && snap_next) {
+                    const float zs = last_in_run ? 0.f : zr;
+                    const uint32_t hi = pack_bf16(zs, 0.f);
+                    const uint32_t lo = pack_bf16(zs - bf_lo(hi), 0.f);
+                    *reinterpret_cast<uint16_t*>(snap_z(b ^ 1) + sw128_offset(0, srow)) = (uint16_t)hi;
+                    *reinterpret_cast<uint16_t*>(snap_z(b ^ 1) + sw128_offset(1, srow)) = (uint16_t)lo;
                 }
-                z_run += __uint_as_float(rz[0]);
             }
             tc_fence_before();
-            if (last_in_run) {
-                // Final state of the head if its last chunk is here; the next run
-                // (if any) starts a new head from zero.
-                if (ch == part.nchunks - 1 && sowner) {
-                    if (S_out) {
-                        float4* dst = reinterpret_cast<float4*>(
-                            S_out + ((int64_t)h * kD + srow) * kD + 32 * g);
-#pragma unroll
-                        for (int qd = 0; qd < 8; ++qd)
-                            dst[qd] = make_float4(S_run[4 * qd], S_run[4 * qd + 1],
-                                                  S_run[4 * qd + 2], S_run[4 * qd + 3]);
-                    }
-                    if (z_out && g == 0) z_out[(int64_t)h * kD + srow] = z_run;
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) S_run[e] = 0.f;
-                z_run = 0.f;
-            }
-            if (i + 1 < nch) write_snap(b ^ 1);
-            if (t == 0) tma_store_wait_read<1>();  // staging buffer b is free again
             fence_proxy_async_smem();
-            ok = named_bar_and(1, kMath, ok);
+            if (t == 0) tma_store_wait_read<0>();  // the output staging tile is free again
+            ok = named_bar_and(3, 128, ok);
             if (!ok) break;
             if (t == 0) {
-                mbar_arrive(&m.p_ready[b]);
-                if (i + 1 < nch) mbar_arrive(&m.s_ready[b ^ 1]);
+                mbar_arrive(&m.ds_free);
+                if (snap_next) mbar_arrive(&m.snap_full[b ^ 1]);
             }
 
-            // (a) of the next chunk while the tensor core finishes this one.
-            if (i + 1 < nch && !(ok = phase_a(i + 1))) break;
-
-            // (c) num / (den + eps) -> bf16 -> staging tile -> TMA store.
-            ok = mbar_wait(&m.mma2_done[b], par, max_spin);
+            // Output: num / (den + eps) -> bf16 -> staging tile -> TMA store.
+            ok = mbar_wait(&m.o_full[b], pb, max_spin);
             tc_fence_after();
+            const uint32_t tO = tmem + kTmO + kTmOStride * b;
+            float inv;
             {
-                uint32_t r0[16], r1[16], rd[16];
-                tmem_ld16(tO + lane_base + 32 * g, r0);
-                tmem_ld16(tO + lane_base + 32 * g + 16, r1);
+                uint32_t rd[16];
                 tmem_ld16(tO + lane_base + 64, rd);
                 tmem_ld_wait();
-                const float inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
-                uint8_t* ot = ostage(b);
+                inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
+            }
 #pragma unroll
-                for (int hq = 0; hq < 4; ++hq) {
-                    const uint32_t* r = hq < 2 ? r0 : r1;
-                    const int e0 = 8 * (hq & 1);
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tO + lane_base + 32 * c2, r0);
+                tmem_ld16(tO + lane_base + 32 * c2 + 16, r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* rr = c < 2 ? r0 : r1;
+                    const int e0 = 8 * (c & 1);
                     uint4 v = make_uint4(
-                        pack_bf16(__uint_as_float(r[e0]) * inv, __uint_as_float(r[e0 + 1]) * inv),
-                        pack_bf16(__uint_as_float(r[e0 + 2]) * inv, __uint_as_float(r[e0 + 3]) * inv),
-                        pack_bf16(__uint_as_float(r[e0 + 4]) * inv, __uint_as_float(r[e0 + 5]) * inv),
-                        pack_bf16(__uint_as_float(r[e0 + 6]) * inv, __uint_as_float(r[e0 + 7]) * inv));
-                    *reinterpret_cast<uint4*>(ot + sw128_offset(row, 32 * g + 8 * hq)) = v;
+                        pack_bf16(__uint_as_float(rr[e0]) * inv, __uint_as_float(rr[e0 + 1]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 2]) * inv, __uint_as_float(rr[e0 + 3]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 4]) * inv, __uint_as_float(rr[e0 + 5]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 6]) * inv, __uint_as_float(rr[e0 + 7]) * inv));
+                    *reinterpret_cast<uint4*>(ostage + sw128_offset(row, 32 * c2 + 8 * c)) = v;
                 }
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            ok = named_bar_and(1, kMath, ok);
-            if (ok && t == 0) {
+            ok = named_bar_and(3, 128, ok);
+            if (!ok) break;
+            if (t == 0) {
                 mbar_arrive(&m.o_free[b]);
-                tma_store_3d(&omap, ostage(b), 0, ch * kC, h);
+                tma_store_3d(&omap, ostage, 0, ch * kC, h);
                 tma_store_commit();
             }
         }
@@ -689,7 +818,7 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
