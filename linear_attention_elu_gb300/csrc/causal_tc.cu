@@ -319,45 +319,57 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // ======================================================== output kernel
-// Warp roles (14 warps):
-//   warps 0-3   phi:   phi on the Q and K tiles of each landed stage, in place
-//   warps 4-7   mask:  A -> causal mask -> bf16 P (shared memory), per chunk
-//   warps 8-11  state: [dS | dz] -> running state -> next snapshot; then the
-//                      output epilogue num / (den + eps) -> TMA store
-//   warp 12     TMA producer       warp 13  MMA issuer (one thread)
-// The four warps of a role cover the four TMEM lane quarters.
+// Warp roles (18 warps):
+//   warps 0-7   phi:   phi on the Q and K tiles of each landed stage, in place
+//   warps 8-11  mask:  A (fp32, TMEM) -> causal mask -> bf16 P, written back into
+//                      the same TMEM columns (A operand of MMA (4))
+//   warps 12-15 state: running state (TMEM) -> bf16 snapshot for the next
+//                      chunk; then the output epilogue num / (den + eps)
+//   warp 16     TMA producer       warp 17  MMA issuer (one thread)
+// The four warps of the mask and state roles cover the four TMEM lane quarters.
+//
+// Per chunk i (stage s = i mod 3, TMEM buffer b = i mod 2), three contraction
+// groups, each a few wide tcgen05.mma instructions:
+//   (2)   [S^T ; z] += [V | 1]^T phi(K)        M=128 (64 value rows, z row), N=64, K=128 tokens
+//   (1+3) [A | num | den] = phi(Q) [phi(K) | S^T | z_hi z_lo]^T      M=128, N=208, K=64
+//   (4)   [num | den] += P [V | 1]             M=128, N=80, K=128 keys, P read from TMEM
+// (4) of chunk i is issued after (2), (1+3) of chunk i + 1, so that the mask
+// role's work on chunk i overlaps the next chunk's contractions.
 
-constexpr int kOutThreads = 448;
+constexpr int kPhiWarps = 8;
+constexpr int kMaskW0 = kPhiWarps, kStateW0 = kPhiWarps + 4;
+constexpr int kProdW = kStateW0 + 4, kMmaW = kProdW + 1;
+constexpr int kOutThreads = 32 * (kMmaW + 1);
+constexpr int kPhiThreads = 32 * kPhiWarps;
 constexpr int kStages = 3;
-// Shared-memory map (offsets from a 1024-aligned base).
-constexpr uint32_t kStageBytes = 3 * kTileBytes;               // Q, K, V tiles
-constexpr uint32_t kOffP = kStages * kStageBytes;              // masked A, bf16, 2 sub-tiles
-constexpr uint32_t kSnapS = kD * 128;                          // S snapshot: 64 rows x 128 B
-constexpr uint32_t kSnapZ = 16 * 128;                          // z tile: 16 rows x 128 B (K-major)
-constexpr uint32_t kSnapBytes = kSnapS + kSnapZ;
-constexpr uint32_t kOffSnap = kOffP + 2 * kTileBytes;          // 2 x (S | z)
-constexpr uint32_t kOffOnes = kOffSnap + 2 * kSnapBytes;       // ones: 16 rows x 128 keys, K-major
-constexpr uint32_t kOnesBytes = 2 * 16 * 128;
-constexpr uint32_t kOffO = kOffOnes + kOnesBytes;              // output staging tile
+// Shared-memory map (offsets from a 1024-aligned base). A stage holds the Q, K
+// and V tiles and, right after K, the snapshot rows S^T (64) and z (16) that
+// complete the K-major operand [phi(K) | S^T | z] of MMA (1+3).
+constexpr uint32_t kStQ = 0, kStK = kTileBytes, kStS = 2 * kTileBytes;
+constexpr uint32_t kStZ = kStS + kD * 128, kStV = kStZ + 16 * 128;
+constexpr uint32_t kStageBytes = kStV + kTileBytes;            // 58 KB
+constexpr uint32_t kOffOnes = kStages * kStageBytes;           // [V | 1] second atom, MN-major
+constexpr uint32_t kOffO = kOffOnes + kTileBytes;              // output staging tile
 constexpr uint32_t kSmemEnd = kOffO + kTileBytes;
 constexpr size_t kOutSmem = 1024 + kSmemEnd;
-// TMEM columns: A[b] at 128 b; O[b] = [num 64 | den 16] at 256 + 96 b; dS = [dS 64 | dz 16] at 432.
-constexpr uint32_t kTmO = 256, kTmOStride = 96, kTmS = 432;
+// TMEM columns: buffer b = [A / P | num | den] at 224 b (208 columns);
+// running state [S^T ; z] at 448 (64 columns, lanes 0-63 = S^T rows, lane 64 = z).
+constexpr uint32_t kTmBuf = 224, kTmState = 448;
 
 struct OutMisc {
-    uint64_t full[kStages], phi_done[kStages], empty[kStages];
-    uint64_t a_full[2], a_free[2], o_full[2], o_free[2], snap_full[2];
-    uint64_t p_full, p_free, ds_full, ds_free, state_init, mma_drain;
+    uint64_t full[kStages], phi_done[kStages], empty[kStages], snap_full[kStages];
+    uint64_t a_full[2], o_full[2], o_free[2];
+    uint64_t p_full, ds_full, mma_drain;
     uint32_t tmem_slot;
 };
 
-// K-major "ones" operand: row 0 = 1.0 over 128 keys (two 64-key sub-tiles), rows 1-15 = 0.
-__device__ __forceinline__ void init_ones_kmajor(uint8_t* t, int tid, int nthreads) {
-    for (int idx = tid; idx < 2 * 16 * 8; idx += nthreads) {
-        const int sub = idx / 128, r = (idx / 8) % 16, pc = idx % 8;
-        const uint32_t one = r == 0 ? 0x3F803F80u : 0u;
-        *reinterpret_cast<uint4*>(t + sub * 2048 + r * 128 + pc * 16) = make_uint4(one, one, one, one);
-    }
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -376,12 +388,7 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
     const int cta = blockIdx.x;
     const int64_t u0 = part.begin(cta), u1 = part.begin(cta + 1);
     const int nch = (int)(u1 - u0);
-    auto stage_q = [&](int s) { return base + s * kStageBytes; };
-    auto stage_k = [&](int s) { return base + s * kStageBytes + kTileBytes; };
-    auto stage_v = [&](int s) { return base + s * kStageBytes + 2 * kTileBytes; };
-    uint8_t* sP = base + kOffP;
-    auto snap_s = [&](int b) { return base + kOffSnap + b * kSnapBytes; };
-    auto snap_z = [&](int b) { return base + kOffSnap + b * kSnapBytes + kSnapS; };
+    auto stage = [&](int s) { return base + s * kStageBytes; };
     uint8_t* ones = base + kOffOnes;
     uint8_t* ostage = base + kOffO;
 
@@ -390,35 +397,31 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
             mbar_init(&m.full[s], 1);
             mbar_init(&m.phi_done[s], 1);
             mbar_init(&m.empty[s], 1);
+            mbar_init(&m.snap_full[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&m.a_full[b], 1);
-            mbar_init(&m.a_free[b], 1);
             mbar_init(&m.o_full[b], 1);
             mbar_init(&m.o_free[b], 1);
-            mbar_init(&m.snap_full[b], 1);
         }
         mbar_init(&m.p_full, 1);
-        mbar_init(&m.p_free, 1);
         mbar_init(&m.ds_full, 1);
-        mbar_init(&m.ds_free, 1);
-        mbar_init(&m.state_init, 1);
         mbar_init(&m.mma_drain, 1);
         fence_mbar_init();
     }
-    if (warp < 12) {
-        init_ones_kmajor(ones, tid, 384);
-        for (int idx = tid; idx < 2 * (int)kSnapZ / 16; idx += 384) {  // both z tiles
-            const int b = idx / (kSnapZ / 16), r = idx % (kSnapZ / 16);
-            *reinterpret_cast<uint4*>(snap_z(b) + r * 16) = make_uint4(0, 0, 0, 0);
+    if (warp < kProdW) {
+        init_ones_tile(ones, tid, 32 * kProdW);
+        for (int idx = tid; idx < kStages * 128; idx += 32 * kProdW) {  // z rows of every stage
+            const int s = idx / 128, r = idx % 128;
+            *reinterpret_cast<uint4*>(stage(s) + kStZ + r * 16) = make_uint4(0, 0, 0, 0);
         }
     }
     fence_proxy_async_smem();
-    if (warp == 13) {
+    if (warp == kMmaW) {
         tmem_alloc(&m.tmem_slot, 512);
         tmem_relinquish();
     }
-    if (warp == 12 && lane == 0) {
+    if (warp == kProdW && lane == 0) {
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
@@ -431,7 +434,7 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
 
-    if (warp == 12) {
+    if (warp == kProdW) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             int i = 0;
@@ -446,350 +449,170 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
                 const int64_t u = u0 + i;
                 const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
                 mbar_arrive_expect_tx(&m.full[s], 3 * kTileBytes);
-                tma_load_3d(stage_q(s), &qmap, &m.full[s], 0, ch * kC, h);
-                tma_load_3d(stage_k(s), &kmap, &m.full[s], 0, ch * kC, h);
-                tma_load_3d(stage_v(s), &vmap, &m.full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + kStQ, &qmap, &m.full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + kStK, &kmap, &m.full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + kStV, &vmap, &m.full[s], 0, ch * kC, h);
             }
             for (int j = i - kStages > 0 ? i - kStages : 0; j < i; ++j)
                 mbar_wait(&m.full[j % kStages], (j / kStages) & 1, kDefaultMaxSpin);
         }
-    } else if (warp == 13) {
+    } else if (warp == kMmaW) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t id_kv = idesc_bf16_f32(64, 64, true, true);
-            const uint32_t id_k1 = idesc_bf16_f32(64, 16, true, false);
-            const uint32_t id_o = idesc_bf16_f32(128, 64, false, true);
-            const uint32_t id_o1 = idesc_bf16_f32(128, 16, false, false);
-            const uint32_t onesa = smem_u32(ones), pa = smem_u32(sP);
-            const uint32_t tS = tmem + kTmS;
-            for (int i = 0; i < nch; ++i) {
-                const int s = i % kStages, b = i & 1;
-                const uint32_t pb = (i >> 1) & 1, pi = i & 1;
-                const uint32_t tA = tmem + 128u * b, tO = tmem + kTmO + kTmOStride * b;
-                if (!mbar_wait(&m.phi_done[s], (i / kStages) & 1, max_spin)) { report_timeout(hdr); break; }
-                if (i >= 2 && !mbar_wait(&m.a_free[b], pb ^ 1, max_spin)) { report_timeout(hdr); break; }
+            const uint32_t id_s = idesc_bf16_f32(128, 64, true, true);     // (2)
+            const uint32_t id_qk = idesc_bf16_f32(128, 208, false, false); // (1+3)
+            const uint32_t id_pv = idesc_bf16_f32(128, 80, false, true);   // (4)
+            const uint32_t onesa = smem_u32(ones);
+            // (4) for chunk j: [num | den] += P_j [V_j | 1].
+            auto issue_pv = [&](int j) -> bool {
+                if (!mbar_wait(&m.p_full, j & 1, max_spin)) return false;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(stage_q(s)), ka = smem_u32(stage_k(s)),
-                               va = smem_u32(stage_v(s));
-                // (1) A = phi(Q) phi(K)^T: M=128 queries, N=128 keys, K=64 features.
+                const int sj = j % kStages, bj = j & 1;
+                const uint32_t va = smem_u32(stage(sj) + kStV);
+                const uint32_t lbo = onesa - va;
+                const uint32_t tbuf = tmem + kTmBuf * bj;
+#pragma unroll
+                for (int k16 = 0; k16 < kC / 16; ++k16)
+                    mma_bf16_ts(tbuf + 128, tbuf + 8 * k16,
+                                smem_desc(va + k16 * 2048, lbo, 1024, kSwizzle128B), id_pv, 1u);
+                mma_commit(&m.o_full[bj]);
+                mma_commit(&m.empty[sj]);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int s = i % kStages, b = i & 1;
+                const uint32_t ps = (i / kStages) & 1;
+                if (!mbar_wait(&m.phi_done[s], ps, max_spin) ||
+                    !mbar_wait(&m.snap_full[s], ps, max_spin)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t qa = smem_u32(stage(s) + kStQ), ka = smem_u32(stage(s) + kStK),
+                               va = smem_u32(stage(s) + kStV);
+                const uint32_t lbo = onesa - va;
+                const bool fresh = (i > 0) && ((u0 + i) % part.nchunks == 0);
+                // (2) running state [S^T ; z] += [V | 1]^T phi(K)  (A MN-major over 2 atoms).
+#pragma unroll
+                for (int k16 = 0; k16 < kC / 16; ++k16)
+                    mma_bf16(tmem + kTmState,
+                             smem_desc(va + k16 * 2048, lbo, 1024, kSwizzle128B),
+                             smem_desc(ka + k16 * 2048, 1024, 1024, kSwizzle128B), id_s,
+                             (fresh && k16 == 0) ? 0u : 1u);
+                mma_commit(&m.ds_full);
+                // (1+3) overwrites buffer b: the output epilogue of chunk i - 2 must be done.
+                if (i >= 2 && !mbar_wait(&m.o_free[b], ((i >> 1) - 1) & 1, max_spin)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // (1+3) [A | num | den] = phi(Q) [phi(K) | S^T | z]^T (B K-major, 208 rows).
 #pragma unroll
                 for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tA, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
+                    mma_bf16(tmem + kTmBuf * b,
+                             smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
                              smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_qk, k16 > 0);
                 mma_commit(&m.a_full[b]);
-                // (2) S += phi(K)^T V (M=64, N=64) and (2b) z += phi(K)^T 1 (N=16), K=128
-                // tokens: the running state [S | z] of the current run lives in TMEM. The
-                // first run starts from the state written by the state role; a later run
-                // starts a new head from zero.
-                const int64_t u = u0 + i;
-                const bool run_start = (u % part.nchunks == 0);
-                if (i == 0 && !mbar_wait(&m.state_init, 0, max_spin)) { report_timeout(hdr); break; }
-                if (i >= 1 && !mbar_wait(&m.ds_free, pi ^ 1, max_spin)) { report_timeout(hdr); break; }
-                tc_fence_after();
-                const bool fresh = (i > 0 && run_start);
-#pragma unroll
-                for (int k16 = 0; k16 < kC / 16; ++k16) {
-                    const uint64_t kd = smem_desc(ka + k16 * 2048, 1024, 1024, kSwizzle128B);
-                    const uint32_t acc = (fresh && k16 == 0) ? 0u : 1u;
-                    mma_bf16(tS, kd, smem_desc(va + k16 * 2048, 1024, 1024, kSwizzle128B), id_kv,
-                             acc);
-                    mma_bf16(tS + 64, kd,
-                             smem_desc(onesa + (k16 >> 2) * 2048 + (k16 & 3) * 32, 16, 1024,
-                                       kSwizzle128B),
-                             id_k1, acc);
-                }
-                mma_commit(&m.ds_full);
-                // (3) num = phi(Q) S_prev and (3b) den = phi(Q) [z_hi; z_lo]: needs the snapshot, free O.
-                if (!mbar_wait(&m.snap_full[b], pb, max_spin)) { report_timeout(hdr); break; }
-                if (i >= 2 && !mbar_wait(&m.o_free[b], pb ^ 1, max_spin)) { report_timeout(hdr); break; }
-                tc_fence_after();
-                const uint32_t sa = smem_u32(snap_s(b)), za = smem_u32(snap_z(b));
-#pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16) {
-                    const uint64_t qd = smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B);
-                    mma_bf16(tO, qd, smem_desc(sa + k16 * 2048, 1024, 1024, kSwizzle128B), id_o,
-                             k16 > 0);
-                    mma_bf16(tO + 64, qd, smem_desc(za + k16 * 32, 16, 1024, kSwizzle128B), id_o1,
-                             k16 > 0);
-                }
-                // (4) num += P V and (4b) den += P 1: K = 128 keys (P in two 64-key sub-tiles).
-                if (!mbar_wait(&m.p_full, pi, max_spin)) { report_timeout(hdr); break; }
-                tc_fence_after();
-#pragma unroll
-                for (int k16 = 0; k16 < kC / 16; ++k16) {
-                    const uint64_t pd = smem_desc(pa + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16,
-                                                  1024, kSwizzle128B);
-                    mma_bf16(tO, pd, smem_desc(va + k16 * 2048, 1024, 1024, kSwizzle128B), id_o, 1u);
-                    mma_bf16(tO + 64, pd,
-                             smem_desc(onesa + (k16 >> 2) * 2048 + (k16 & 3) * 32, 16, 1024,
-                                       kSwizzle128B),
-                             id_o1, 1u);
-                }
-                mma_commit(&m.o_full[b]);
-                mma_commit(&m.p_free);
-                mma_commit(&m.empty[s]);
+                if (i >= 1 && !issue_pv(i - 1)) ok = false;
             }
+            if (ok && nch > 0 && !issue_pv(nch - 1)) ok = false;
+            if (!ok) report_timeout(hdr);
             mma_commit(&m.mma_drain);  // every issued MMA completes before TMEM is released
             mbar_wait(&m.mma_drain, 0, kDefaultMaxSpin);
         }
-    } else if (warp < 4) {
+    } else if (warp < kMaskW0) {
         // ---------------------------------------------------------- phi role
-        const int t = tid;  // 0..127
+        const int t = tid;  // 0 .. kPhiThreads - 1
         bool ok = true;
         for (int i = 0; i < nch; ++i) {
             const int s = i % kStages;
             const int ch = (int)((u0 + i) % part.nchunks);
             const int valid = min(kC, N - ch * kC);
             ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
-            uint8_t* qt = stage_q(s);
-            uint8_t* kt = stage_k(s);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint4 vq[4], vk[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = (t >> 3) + 16 * (4 * half + k);
-                    vq[k] = *reinterpret_cast<const uint4*>(qt + r * 128 + (t & 7) * 16);
-                    vk[k] = *reinterpret_cast<const uint4*>(kt + r * 128 + (t & 7) * 16);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = (t >> 3) + 16 * (4 * half + k);
-                    *reinterpret_cast<uint4*>(qt + r * 128 + (t & 7) * 16) = phi8(vq[k]);
-                    *reinterpret_cast<uint4*>(kt + r * 128 + (t & 7) * 16) =
-                        r < valid ? phi8(vk[k]) : make_uint4(0, 0, 0, 0);
-                }
-            }
+            phi_tile_256(stage(s) + kStQ, t, kC);
+            phi_tile_256(stage(s) + kStK, t, valid);
             fence_proxy_async_smem();
-            ok = named_bar_and(1, 128, ok);
+            ok = named_bar_and(1, kPhiThreads, ok);
             if (!ok) break;
             if (t == 0) mbar_arrive(&m.phi_done[s]);
         }
         if (!ok && t == 0) report_timeout(hdr);
-    } else if (warp < 8) {
+    } else if (warp < kStateW0) {
         // ---------------------------------------------------------- mask role
-        const int row = 32 * q4 + lane;  // query row
-        const int t = tid - 128;
+        // A block j (32 keys, columns 32j..32j+31) -> P block j (16 packed columns
+        // 16j..16j+15) in the same TMEM buffer; in increasing j every A column is
+        // read before the P columns that cover it are written.
+        const int t = tid - 32 * kMaskW0;
         bool ok = true;
         for (int i = 0; i < nch; ++i) {
             const int b = i & 1;
-            const uint32_t pb = (i >> 1) & 1;
-            const uint32_t tA = tmem + 128u * b;
-            ok = mbar_wait(&m.a_full[b], pb, max_spin);
-            if (i >= 1) ok = mbar_wait(&m.p_free, (i - 1) & 1, max_spin) && ok;
+            const uint32_t tbuf = tmem + kTmBuf * b + lane_base;
+            ok = mbar_wait(&m.a_full[b], (i >> 1) & 1, max_spin);
             tc_fence_after();
-            // Key block j (32 keys): j < q4 fully visible, j == q4 holds the diagonal, j > q4 masked.
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint8_t* pt = sP + (j >> 1) * kTileBytes;
-                const int col0 = 32 * (j & 1);
+                uint32_t p[16];
                 if (j > q4) {
+                    // Queries of this lane quarter see no key of block j.
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(pt + sw128_offset(row, col0 + 8 * c)) =
-                            make_uint4(0, 0, 0, 0);
-                    continue;
-                }
-                uint32_t r0[16], r1[16];
-                tmem_ld16(tA + lane_base + 32 * j, r0);
-                tmem_ld16(tA + lane_base + 32 * j + 16, r1);
-                tmem_ld_wait();
-                float a[32];
+                    for (int e = 0; e < 16; ++e) p[e] = 0u;
+                } else {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tbuf + 32 * j, r0);
+                    tmem_ld16(tbuf + 32 * j + 16, r1);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    a[e] = __uint_as_float(r0[e]);
-                    a[16 + e] = __uint_as_float(r1[e]);
+                    for (int e = 0; e < 8; ++e) {
+                        float a0 = __uint_as_float(r0[2 * e]), a1 = __uint_as_float(r0[2 * e + 1]);
+                        float c0 = __uint_as_float(r1[2 * e]), c1 = __uint_as_float(r1[2 * e + 1]);
+                        if (j == q4) {  // block holding the diagonal: key 32 q4 + e' <= row 32 q4 + lane
+                            a0 = (2 * e <= lane) ? a0 : 0.f;
+                            a1 = (2 * e + 1 <= lane) ? a1 : 0.f;
+                            c0 = (16 + 2 * e <= lane) ? c0 : 0.f;
+                            c1 = (17 + 2 * e <= lane) ? c1 : 0.f;
+                        }
+                        p[e] = pack_bf16(a0, a1);
+                        p[8 + e] = pack_bf16(c0, c1);
+                    }
                 }
-                if (j == q4) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = (e <= lane) ? a[e] : 0.f;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 v = make_uint4(pack_bf16(a[8 * c], a[8 * c + 1]),
-                                         pack_bf16(a[8 * c + 2], a[8 * c + 3]),
-                                         pack_bf16(a[8 * c + 4], a[8 * c + 5]),
-                                         pack_bf16(a[8 * c + 6], a[8 * c + 7]));
-                    *reinterpret_cast<uint4*>(pt + sw128_offset(row, col0 + 8 * c)) = v;
-                }
+                tmem_st16(tbuf + 16 * j, p);
             }
+            tmem_st_wait();
             tc_fence_before();
-            fence_proxy_async_smem();
             ok = named_bar_and(2, 128, ok);
             if (!ok) break;
-            if (t == 0) {
-                mbar_arrive(&m.a_free[b]);
-                mbar_arrive(&m.p_full);
-            }
+            if (t == 0) mbar_arrive(&m.p_full);
         }
         if (!ok && t == 0) report_timeout(hdr);
     } else {
         // ---------------------------------------------------------- state + output role
-        // The running state [S | z] is accumulated in TMEM by the MMAs (2), (2b)
-        // (M = 64 layout: state row r in lane 32 (r / 16) + r % 16). This role
-        // writes the first run's start state, reads the state after every chunk
-        // into the bf16 snapshot used by the next chunk's MMA (3), and writes the
-        // outputs.
-        const int t = tid - 256;                    // 0..127
-        const int row = 32 * q4 + lane;             // query row (M = 128 layout)
-        const int srow = 16 * q4 + (lane & 15);     // state row (M = 64 layout), lanes < 16
-        const bool sowner = lane < 16;
-        const uint32_t tS = tmem + kTmS + lane_base;
+        const int t = tid - 32 * kStateW0;       // 0..127
+        const int row = 32 * q4 + lane;          // TMEM lane: S^T row (< 64), z row (64), query row
+        const uint32_t tS = tmem + kTmState + lane_base;
 
-        // Start state of the first run: sum of the aggregates of this head's
-        // chunks held by lower-numbered CTAs (written by the state kernel), into
-        // TMEM and into snapshot 0.
-        pdl_wait();  // the state kernel's aggregates are complete and visible
-        {
-            const int h = (int)(u0 / part.nchunks);
-            const int64_t head_begin = (int64_t)h * part.nchunks;
-            float S0[kD];
-            float z0 = 0.f;
-#pragma unroll
-            for (int e = 0; e < kD; ++e) S0[e] = 0.f;
-            if (u0 > head_begin && sowner) {
-                for (int c2 = cta - 1; c2 >= 0; --c2) {
-                    const int64_t b0 = part.begin(c2), b1 = part.begin(c2 + 1);
-                    if (b1 <= head_begin) break;
-                    if (b1 <= b0) continue;
-                    const int r = (int)(h - b0 / part.nchunks);
-                    const float* a = agg + ((int64_t)c2 * part.maxr + r) * kE;
-                    const float4* src = reinterpret_cast<const float4*>(a + srow * kD);
-#pragma unroll
-                    for (int qd = 0; qd < kD / 4; ++qd) {
-                        float4 v = src[qd];
-                        S0[4 * qd] += v.x;
-                        S0[4 * qd + 1] += v.y;
-                        S0[4 * qd + 2] += v.z;
-                        S0[4 * qd + 3] += v.w;
-                    }
-                    z0 += a[kD * kD + srow];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(S0[16 * c + e]);
-                tmem_st16(tS + 16 * c, w);
-            }
-            {
-                uint32_t w[16];
-                w[0] = __float_as_uint(z0);
-#pragma unroll
-                for (int e = 1; e < 16; ++e) w[e] = 0u;
-                tmem_st16(tS + 64, w);
-            }
-            tmem_st_wait();
-            if (sowner) {
-                uint8_t* d = snap_s(0);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = make_uint4(pack_bf16(S0[8 * c], S0[8 * c + 1]),
-                                         pack_bf16(S0[8 * c + 2], S0[8 * c + 3]),
-                                         pack_bf16(S0[8 * c + 4], S0[8 * c + 5]),
-                                         pack_bf16(S0[8 * c + 6], S0[8 * c + 7]));
-                    *reinterpret_cast<uint4*>(d + sw128_offset(srow, 8 * c)) = v;
-                }
-                const uint32_t hi = pack_bf16(z0, 0.f);
-                const uint32_t lo = pack_bf16(z0 - bf_lo(hi), 0.f);
-                *reinterpret_cast<uint16_t*>(snap_z(0) + sw128_offset(0, srow)) = (uint16_t)hi;
-                *reinterpret_cast<uint16_t*>(snap_z(0) + sw128_offset(1, srow)) = (uint16_t)lo;
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            named_bar(3, 128);
-            if (t == 0) {
-                mbar_arrive(&m.state_init);
-                mbar_arrive(&m.snap_full[0]);
-            }
-        }
-        bool ok = true;
-        for (int i = 0; i < nch; ++i) {
-            const int b = i & 1;
-            const uint32_t pb = (i >> 1) & 1;
-            const int64_t u = u0 + i;
+        // Output epilogue for chunk j: num / (den + eps) -> bf16 -> staging -> TMA store.
+        auto output = [&](int j) -> bool {
+            const int bj = j & 1;
+            const int64_t u = u0 + j;
             const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
-            const bool last_in_run = (u + 1 == u1) || ((u + 1) / part.nchunks != h);
-            const bool head_end = (ch == part.nchunks - 1);
-
-            // State after chunk i -> snapshot for chunk i + 1 (zero when a new head starts).
-            ok = mbar_wait(&m.ds_full, i & 1, max_spin);
+            bool okj = mbar_wait(&m.o_full[bj], (j >> 1) & 1, max_spin);
+            if (t == 0) tma_store_wait_read<0>();  // the staging tile is free again
+            named_bar(3, 128);
             tc_fence_after();
-            const bool snap_next = (i + 1 < nch);
-            uint8_t* dnext = snap_s(b ^ 1);
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t r0[16], r1[16];
-                tmem_ld16(tS + 32 * c2, r0);
-                tmem_ld16(tS + 32 * c2 + 16, r1);
-                tmem_ld_wait();
-                if (sowner && last_in_run && head_end && S_out) {
-                    float4* dst = reinterpret_cast<float4*>(S_out + ((int64_t)h * kD + srow) * kD + 32 * c2);
-#pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) {
-                        dst[qd] = make_float4(__uint_as_float(r0[4 * qd]), __uint_as_float(r0[4 * qd + 1]),
-                                              __uint_as_float(r0[4 * qd + 2]), __uint_as_float(r0[4 * qd + 3]));
-                        dst[qd + 4] = make_float4(__uint_as_float(r1[4 * qd]), __uint_as_float(r1[4 * qd + 1]),
-                                                  __uint_as_float(r1[4 * qd + 2]), __uint_as_float(r1[4 * qd + 3]));
-                    }
-                }
-                if (sowner && snap_next) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t* rr = c < 2 ? r0 : r1;
-                        const int e0 = 8 * (c & 1);
-                        uint4 v = last_in_run
-                                      ? make_uint4(0, 0, 0, 0)
-                                      : make_uint4(pack_bf16(__uint_as_float(rr[e0]), __uint_as_float(rr[e0 + 1])),
-                                                   pack_bf16(__uint_as_float(rr[e0 + 2]), __uint_as_float(rr[e0 + 3])),
-                                                   pack_bf16(__uint_as_float(rr[e0 + 4]), __uint_as_float(rr[e0 + 5])),
-                                                   pack_bf16(__uint_as_float(rr[e0 + 6]), __uint_as_float(rr[e0 + 7])));
-                        *reinterpret_cast<uint4*>(dnext + sw128_offset(srow, 32 * c2 + 8 * c)) = v;
-                    }
-                }
-            }
-            {
-                uint32_t rz[16];
-                tmem_ld16(tS + 64, rz);
-                tmem_ld_wait();
-                const float zr = __uint_as_float(rz[0]);
-                if (sowner && last_in_run && head_end && z_out) z_out[(int64_t)h * kD + srow] = zr;
-                if (sowner && snap_next) {
-                    const float zs = last_in_run ? 0.f : zr;
-                    const uint32_t hi = pack_bf16(zs, 0.f);
-                    const uint32_t lo = pack_bf16(zs - bf_lo(hi), 0.f);
-                    *reinterpret_cast<uint16_t*>(snap_z(b ^ 1) + sw128_offset(0, srow)) = (uint16_t)hi;
-                    *reinterpret_cast<uint16_t*>(snap_z(b ^ 1) + sw128_offset(1, srow)) = (uint16_t)lo;
-                }
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            if (t == 0) tma_store_wait_read<0>();  // the output staging tile is free again
-            ok = named_bar_and(3, 128, ok);
-            if (!ok) break;
-            if (t == 0) {
-                mbar_arrive(&m.ds_free);
-                if (snap_next) mbar_arrive(&m.snap_full[b ^ 1]);
-            }
-
-            // Output: num / (den + eps) -> bf16 -> staging tile -> TMA store.
-            ok = mbar_wait(&m.o_full[b], pb, max_spin);
-            tc_fence_after();
-            const uint32_t tO = tmem + kTmO + kTmOStride * b;
+            const uint32_t to = tmem + kTmBuf * bj + 128 + lane_base;
             float inv;
             {
                 uint32_t rd[16];
-                tmem_ld16(tO + lane_base + 64, rd);
+                tmem_ld16(to + 64, rd);
                 tmem_ld_wait();
                 inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
             }
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t r0[16], r1[16];
-                tmem_ld16(tO + lane_base + 32 * c2, r0);
-                tmem_ld16(tO + lane_base + 32 * c2 + 16, r1);
+                tmem_ld16(to + 32 * c2, r0);
+                tmem_ld16(to + 32 * c2 + 16, r1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -805,20 +628,145 @@ causal_output_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            ok = named_bar_and(3, 128, ok);
-            if (!ok) break;
-            if (t == 0) {
-                mbar_arrive(&m.o_free[b]);
+            okj = named_bar_and(3, 128, okj);
+            if (okj && t == 0) {
+                mbar_arrive(&m.o_free[bj]);
                 tma_store_3d(&omap, ostage, 0, ch * kC, h);
                 tma_store_commit();
             }
+            return okj;
+        };
+        // Snapshot rows for chunk j (stage j mod 3): S^T row `row` (rows < 64) and
+        // z_hi, z_lo (row 64), from 64 fp32 values v[] of this TMEM lane.
+        auto write_snap_half = [&](uint8_t* st, int c2, const uint32_t (&r0)[16],
+                                   const uint32_t (&r1)[16], bool zero) {
+            if (row < kD) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* rr = c < 2 ? r0 : r1;
+                    const int e0 = 8 * (c & 1);
+                    uint4 v = zero ? make_uint4(0, 0, 0, 0)
+                                   : make_uint4(pack_bf16(__uint_as_float(rr[e0]), __uint_as_float(rr[e0 + 1])),
+                                                pack_bf16(__uint_as_float(rr[e0 + 2]), __uint_as_float(rr[e0 + 3])),
+                                                pack_bf16(__uint_as_float(rr[e0 + 4]), __uint_as_float(rr[e0 + 5])),
+                                                pack_bf16(__uint_as_float(rr[e0 + 6]), __uint_as_float(rr[e0 + 7])));
+                    *reinterpret_cast<uint4*>(st + kStS + sw128_offset(row, 32 * c2 + 8 * c)) = v;
+                }
+            } else if (row == kD) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* rr = c < 2 ? r0 : r1;
+                    const int e0 = 8 * (c & 1);
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float za = zero ? 0.f : __uint_as_float(rr[e0 + 2 * e]);
+                        const float zb = zero ? 0.f : __uint_as_float(rr[e0 + 2 * e + 1]);
+                        hi[e] = pack_bf16(za, zb);
+                        lo[e] = pack_bf16(za - bf_lo(hi[e]), zb - __uint_as_float(hi[e] & 0xFFFF0000u));
+                    }
+                    *reinterpret_cast<uint4*>(st + kStZ + sw128_offset(0, 32 * c2 + 8 * c)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(st + kStZ + sw128_offset(1, 32 * c2 + 8 * c)) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        };
+
+        // Start state of the first run: sum of the aggregates (S row-major
+        // [feature][value], then z) of this head's chunks held by lower-numbered
+        // CTAs, transposed into TMEM rows (S^T; z) and into the stage-0 snapshot.
+        pdl_wait();  // the state kernel's aggregates are complete and visible
+        {
+            const int h = (int)(u0 / part.nchunks);
+            const int64_t head_begin = (int64_t)h * part.nchunks;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r0[16], r1[16];
+                float acc[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                if (u0 > head_begin && row <= kD) {
+                    for (int cb = cta - 1; cb >= 0; --cb) {
+                        const int64_t b0 = part.begin(cb), b1 = part.begin(cb + 1);
+                        if (b1 <= head_begin) break;
+                        if (b1 <= b0) continue;
+                        const float* a = agg + ((int64_t)cb * part.maxr + (h - b0 / part.nchunks)) * kE;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int c = 32 * c2 + e;  // feature index
+                            acc[e] += row < kD ? a[c * kD + row] : a[kD * kD + c];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    r0[e] = __float_as_uint(acc[e]);
+                    r1[e] = __float_as_uint(acc[16 + e]);
+                }
+                tmem_st16(tS + 32 * c2, r0);
+                tmem_st16(tS + 32 * c2 + 16, r1);
+                write_snap_half(stage(0), c2, r0, r1, false);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(3, 128);
+            if (t == 0) mbar_arrive(&m.snap_full[0]);
         }
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
+            const int64_t u = u0 + i;
+            const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
+            const bool last_in_run = (u + 1 == u1) || ((u + 1) / part.nchunks != h);
+            const bool head_end = (ch == part.nchunks - 1);
+            const bool snap_next = (i + 1 < nch);
+            uint8_t* nst = stage((i + 1) % kStages);
+
+            // State after chunk i -> snapshot for chunk i + 1 (zero when a new head starts).
+            ok = mbar_wait(&m.ds_full, i & 1, max_spin);
+            tc_fence_after();
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tS + 32 * c2, r0);
+                tmem_ld16(tS + 32 * c2 + 16, r1);
+                tmem_ld_wait();
+                if (last_in_run && head_end) {
+                    // Final state of the head: S[c][n] (row n of S^T holds column n of S), z.
+                    if (row < kD && S_out) {
+                        float* dst = S_out + (int64_t)h * kD * kD + row;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            dst[(32 * c2 + e) * kD] = __uint_as_float(r0[e]);
+                            dst[(32 * c2 + 16 + e) * kD] = __uint_as_float(r1[e]);
+                        }
+                    } else if (row == kD && z_out) {
+                        float* dst = z_out + (int64_t)h * kD + 32 * c2;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            dst[e] = __uint_as_float(r0[e]);
+                            dst[16 + e] = __uint_as_float(r1[e]);
+                        }
+                    }
+                }
+                if (snap_next) write_snap_half(nst, c2, r0, r1, last_in_run);
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            ok = named_bar_and(3, 128, ok);
+            if (!ok) break;
+            if (t == 0 && snap_next) mbar_arrive(&m.snap_full[(i + 1) % kStages]);
+            // Output of the previous chunk while the tensor core works on this one.
+            if (i >= 1 && !(ok = output(i - 1))) break;
+        }
+        if (ok && nch > 0) ok = output(nch - 1);
         if (!ok && t == 0) report_timeout(hdr);
         if (t == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 13) {
+    if (warp == kMmaW) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
