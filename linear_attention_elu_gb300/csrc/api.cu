@@ -45,6 +45,7 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
             if (la::tc_causal_supported(Dk, Dv, dt)) return la::tc_causal_workspace(BH, N);
             return la::simt_causal_workspace(BH, N, Dk, Dv);
         case LA_OP_NONCAUSAL:
+            if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N);
             return la::simt_noncausal_workspace(BH, N, Dk, Dv);
         default:
             return 0;
@@ -117,6 +118,8 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
         *launches = 1;
     else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
         *launches = la::tc_causal_launches();
+    else if (op == LA_OP_NONCAUSAL && la::tc_noncausal_supported(Dk, Dv, dt))
+        *launches = 2;
     else
         *launches = 3;
     return LA_OK;
@@ -144,6 +147,9 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
     const size_t need = kHeaderBytes + body_bytes(LA_OP_NONCAUSAL, B, H, N, Dk, Dv, dt);
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
+    if (la::tc_noncausal_supported(Dk, Dv, dt))
+        return from_cuda(la::tc_noncausal(q, k, v, o, BH, N, eps, workspace, body,
+                                          (cudaStream_t)stream));
     return from_cuda(la::simt_noncausal(q, k, v, o, dt, BH, N, Dk, Dv, eps, body,
                                         (cudaStream_t)stream));
 }

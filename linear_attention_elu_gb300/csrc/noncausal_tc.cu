@@ -1,0 +1,536 @@
+// Tensor-core (tcgen05) non-causal forward for bf16 inputs, Dk = Dv = 128.
+//
+// Method ("Why Replace Attention? The Softmax Bottleneck and the Path to Linear
+// Time", section 6.2; "Transformers Are RNNs: Linear Attention", "Reassociate
+// the Products"): per head, S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j),
+// then o_i = phi(q_i)^T S / (phi(q_i)^T z + eps) for every query.
+//
+// Two launches over the persistent-CTA chunk partition (tc_common.cuh):
+//   state kernel  per run (a CTA's chunks of one head): S_run = phi(K)^T V on
+//                 the tensor core (M = 128 features, N = 128 values, fp32 in
+//                 TMEM), z_run = column sums of phi(K) on the CUDA cores, both
+//                 written to the workspace. K and V are read once.
+//   apply kernel  per run: S = sum of the runs of that head (the split-N
+//                 reduction), laid out once in shared memory as the K-major
+//                 operand [S^T | z_hi | z_lo] (144 rows); per chunk of 128
+//                 queries [num | den] = phi(Q) [S^T | z]^T (M = 128, N = 144,
+//                 K = 128), then o = num / (den + eps). Q is read once, O
+//                 written once.
+// The apply kernel is a programmatic dependent of the state kernel.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_util.cuh"
+
+namespace la {
+
+namespace {
+
+using namespace tc;
+using namespace tcc;
+
+constexpr int kD = 128;                     // Dk = Dv
+constexpr int kE = kD * kD + kD;            // floats per aggregate (S row-major [c][n], then z)
+constexpr int kNb = kD + 16;                // B operand rows: S^T, z_hi, z_lo, zero padding
+
+// ======================================================== state kernel
+// Warps 0-7: phi on K (+ z sums) and the read-out of S. Warp 8: TMA. Warp 9: MMA.
+
+constexpr int kSStages = 3;
+constexpr uint32_t kSStage = 4 * kTileBytes;              // K0 K1 V0 V1 (64 KB)
+constexpr size_t kSSmem = 1024 + kSStages * kSStage;
+constexpr int kSThreads = 320;
+
+__global__ void __launch_bounds__(kSThreads, 1)
+nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                float* __restrict__ agg, Partition part, int N, WsHeader* hdr) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t full[kSStages], empty[kSStages], phi_done[kSStages];
+    __shared__ uint64_t run_done, tmem_free, mma_drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float zsum[kD];
+
+    pdl_launch_dependents();
+    const uint32_t max_spin = hdr->max_spin;
+    const bool hold = hdr->hold_item != 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int64_t u0 = part.begin(cta), u1 = part.begin(cta + 1);
+    auto stage = [&](int s) { return base + s * kSStage; };
+
+    if (tid == 0) {
+        for (int s = 0; s < kSStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&phi_done[s], 1);
+        }
+        mbar_init(&run_done, 1);
+        mbar_init(&tmem_free, 1);
+        mbar_init(&mma_drain, 1);
+        fence_mbar_init();
+    }
+    if (tid < kD) zsum[tid] = 0.f;
+    if (warp == 9) {
+        tmem_alloc(&tmem_slot, 128);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 8) {
+        if (lane == 0) {
+            int i = 0;
+            for (int64_t u = u0; u < u1; ++u, ++i) {
+                const int s = i % kSStages;
+                if (i >= kSStages && !mbar_wait(&empty[s], ((i / kSStages) - 1) & 1, max_spin)) {
+                    report_timeout(hdr);
+                    break;
+                }
+                if (hold) break;  // test hook: a load that is never issued
+                const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
+                mbar_arrive_expect_tx(&full[s], 4 * kTileBytes);
+                tma_load_3d(stage(s), &kmap, &full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + kTileBytes, &kmap, &full[s], 64, ch * kC, h);
+                tma_load_3d(stage(s) + 2 * kTileBytes, &vmap, &full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + 3 * kTileBytes, &vmap, &full[s], 64, ch * kC, h);
+            }
+            for (int j = i - kSStages > 0 ? i - kSStages : 0; j < i; ++j)
+                mbar_wait(&full[j % kSStages], (j / kSStages) & 1, kDefaultMaxSpin);
+        }
+    } else if (warp == 9) {
+        if (lane == 0) {
+            // S += phi(K)^T V: A = phi(K) MN-major (two 64-feature atoms), B = V MN-major.
+            const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+            int i = 0, run = 0;
+            bool first_in_run = true, ok = true;
+            for (int64_t u = u0; u < u1; ++u, ++i) {
+                const int s = i % kSStages;
+                const int h = (int)(u / part.nchunks);
+                const bool last_in_run = (u + 1 == u1) || ((u + 1) / part.nchunks != h);
+                if (!mbar_wait(&phi_done[s], (i / kSStages) & 1, max_spin) ||
+                    (first_in_run && run > 0 && !mbar_wait(&tmem_free, (run - 1) & 1, max_spin))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ka = smem_u32(stage(s)), va = smem_u32(stage(s) + 2 * kTileBytes);
+#pragma unroll
+                for (int k16 = 0; k16 < kC / 16; ++k16)
+                    mma_bf16(tmem, smem_desc(ka + k16 * 2048, kTileBytes, 1024, kSwizzle128B),
+                             smem_desc(va + k16 * 2048, kTileBytes, 1024, kSwizzle128B), idesc,
+                             (first_in_run && k16 == 0) ? 0u : 1u);
+                mma_commit(&empty[s]);
+                if (last_in_run) {
+                    mma_commit(&run_done);
+                    ++run;
+                }
+                first_in_run = last_in_run;
+            }
+            if (!ok) report_timeout(hdr);
+            mma_commit(&mma_drain);
+            mbar_wait(&mma_drain, 0, kDefaultMaxSpin);
+        }
+    } else {
+        // Math warps 0-7 (256 threads). Thread t handles physical 16-byte chunk
+        // (t & 7) of rows (t >> 3) + 32 k of each 64-feature box: logical feature
+        // group jgrp = (t & 7) ^ ((t >> 3) & 7), the same for all its rows.
+        const int t = tid;
+        const int jgrp = (t & 7) ^ ((t >> 3) & 7);
+        const int g = warp >> 2, q4 = warp & 3;
+        float zp[2][8];
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zp[bx][e] = 0.f;
+        int i = 0, run = 0;
+        bool ok = true;
+        for (int64_t u = u0; u < u1; ++u, ++i) {
+            const int s = i % kSStages;
+            const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
+            const bool last_in_run = (u + 1 == u1) || ((u + 1) / part.nchunks != h);
+            const int valid = min(kC, N - ch * kC);
+            ok = mbar_wait(&full[s], (i / kSStages) & 1, max_spin);
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx) {
+                uint8_t* kt = stage(s) + bx * kTileBytes;
+                uint4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[k] = *reinterpret_cast<const uint4*>(kt + ((t >> 3) + 32 * k) * 128 + (t & 7) * 16);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (t >> 3) + 32 * k;
+                    uint4 o = make_uint4(0, 0, 0, 0);
+                    if (r < valid) {
+                        o = phi8(v[k]);
+                        const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            zp[bx][2 * e] += bf_lo(w[e]);
+                            zp[bx][2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(kt + r * 128 + (t & 7) * 16) = o;
+                }
+            }
+            fence_proxy_async_smem();
+            ok = named_bar_and(1, 256, ok);
+            if (!ok) break;
+            if (t == 0) mbar_arrive(&phi_done[s]);
+            if (last_in_run) {
+                // z of the run: reduce the column-group partials.
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float vsum = zp[bx][e];
+                        vsum += __shfl_xor_sync(0xffffffffu, vsum, 9);
+                        vsum += __shfl_xor_sync(0xffffffffu, vsum, 18);
+                        if ((lane >> 3) == 0) atomicAdd(&zsum[64 * bx + 8 * jgrp + e], vsum);
+                        zp[bx][e] = 0.f;
+                    }
+                float* out = agg + ((int64_t)cta * part.maxr + run) * kE;
+                ok = mbar_wait(&run_done, run & 1, max_spin);
+                tc_fence_after();
+                // S rows = features: lane 32 q4 + l holds feature row, warpgroup g value columns [64g, 64g+64).
+                const int row = 32 * q4 + lane;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r0[16], r1[16];
+                    const uint32_t ta = tmem + ((uint32_t)(32 * q4) << 16) + 64 * g + 32 * c2;
+                    tmem_ld16(ta, r0);
+                    tmem_ld16(ta + 16, r1);
+                    tmem_ld_wait();
+                    float4* dst = reinterpret_cast<float4*>(out + row * kD + 64 * g + 32 * c2);
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) {
+                        dst[qd] = make_float4(__uint_as_float(r0[4 * qd]), __uint_as_float(r0[4 * qd + 1]),
+                                              __uint_as_float(r0[4 * qd + 2]), __uint_as_float(r0[4 * qd + 3]));
+                        dst[qd + 4] = make_float4(__uint_as_float(r1[4 * qd]), __uint_as_float(r1[4 * qd + 1]),
+                                                  __uint_as_float(r1[4 * qd + 2]), __uint_as_float(r1[4 * qd + 3]));
+                    }
+                }
+                tc_fence_before();
+                ok = named_bar_and(1, 256, ok);   // zsum complete, TMEM read
+                if (!ok) break;
+                if (t < kD) {
+                    out[kD * kD + t] = zsum[t];
+                    zsum[t] = 0.f;
+                }
+                named_bar(1, 256);
+                if (t == 0) mbar_arrive(&tmem_free);
+                ++run;
+            }
+        }
+        if (!ok && t == 0) report_timeout(hdr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ======================================================== apply kernel
+// Warps 0-7: phi on Q. Warps 8-15: operand build (per run) and output epilogue
+// (two warps per TMEM lane quarter, each half the value columns).
+// Warp 16: TMA producer. Warp 17: MMA issuer.
+
+constexpr int kAStages = 3;
+constexpr uint32_t kAStage = 2 * kTileBytes;               // Q0 Q1 (32 KB)
+constexpr uint32_t kBSub = kNb * 128;                      // one 64-feature sub-tile of [S^T | z]
+constexpr uint32_t kOffB = kAStages * kAStage;
+constexpr uint32_t kOffO = kOffB + 2 * kBSub;              // output staging (2 boxes)
+constexpr size_t kASmem = 1024 + kOffO + 2 * kTileBytes;
+constexpr int kAThreads = 576;
+constexpr uint32_t kTmStride = 256;                        // TMEM buffer b at 256 b (144 columns)
+
+struct ApplyMisc {
+    uint64_t full[kAStages], empty[kAStages], phi_done[kAStages];
+    uint64_t o_full[2], o_free[2], b_ready, mma_drain;
+    uint32_t tmem_slot;
+};
+
+__global__ void __launch_bounds__(kAThreads, 1)
+nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                const float* __restrict__ agg, Partition part, float eps, WsHeader* hdr) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ ApplyMisc m;
+    const uint32_t max_spin = hdr->max_spin;
+    const bool hold = hdr->hold_item != 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int64_t u0 = part.begin(cta), u1 = part.begin(cta + 1);
+    const int nch = (int)(u1 - u0);
+    auto stage = [&](int s) { return base + s * kAStage; };
+    uint8_t* bop = base + kOffB;
+    uint8_t* ostage = base + kOffO;
+
+    if (tid == 0) {
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&m.full[s], 1);
+            mbar_init(&m.empty[s], 1);
+            mbar_init(&m.phi_done[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&m.o_full[b], 1);
+            mbar_init(&m.o_free[b], 1);
+        }
+        mbar_init(&m.b_ready, 1);
+        mbar_init(&m.mma_drain, 1);
+        fence_mbar_init();
+    }
+    // Zero the whole operand once (its padding rows stay zero).
+    for (int idx = tid; idx < (int)(2 * kBSub / 16); idx += kAThreads)
+        reinterpret_cast<uint4*>(bop)[idx] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 17) {
+        tmem_alloc(&m.tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == 16 && lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&omap);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = m.tmem_slot;
+
+    if (warp == 16) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int i = 0;
+            for (; i < nch; ++i) {
+                const int s = i % kAStages;
+                if (i >= kAStages && !mbar_wait(&m.empty[s], ((i / kAStages) - 1) & 1, max_spin)) {
+                    report_timeout(hdr);
+                    break;
+                }
+                if (hold) break;  // test hook: a load that is never issued
+                const int64_t u = u0 + i;
+                const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
+                mbar_arrive_expect_tx(&m.full[s], 2 * kTileBytes);
+                tma_load_3d(stage(s), &qmap, &m.full[s], 0, ch * kC, h);
+                tma_load_3d(stage(s) + kTileBytes, &qmap, &m.full[s], 64, ch * kC, h);
+            }
+            for (int j = i - kAStages > 0 ? i - kAStages : 0; j < i; ++j)
+                mbar_wait(&m.full[j % kAStages], (j / kAStages) & 1, kDefaultMaxSpin);
+        }
+    } else if (warp == 17) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, kNb, false, false);
+            const uint32_t ba = smem_u32(bop);
+            int run = 0;
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int s = i % kAStages, b = i & 1;
+                const int64_t u = u0 + i;
+                const bool first_in_run = (i == 0) || (u % part.nchunks == 0);
+                if (!mbar_wait(&m.phi_done[s], (i / kAStages) & 1, max_spin) ||
+                    (first_in_run && !mbar_wait(&m.b_ready, run & 1, max_spin)) ||
+                    (i >= 2 && !mbar_wait(&m.o_free[b], ((i >> 1) - 1) & 1, max_spin))) {
+                    ok = false;
+                    break;
+                }
+                if (first_in_run) ++run;
+                tc_fence_after();
+                const uint32_t qa = smem_u32(stage(s));
+#pragma unroll
+                for (int k16 = 0; k16 < kD / 16; ++k16)
+                    mma_bf16(tmem + kTmStride * b,
+                             smem_desc(qa + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
+                             smem_desc(ba + (k16 >> 2) * kBSub + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
+                             idesc, k16 > 0);
+                mma_commit(&m.o_full[b]);
+                mma_commit(&m.empty[s]);
+            }
+            if (!ok) report_timeout(hdr);
+            mma_commit(&m.mma_drain);
+            mbar_wait(&m.mma_drain, 0, kDefaultMaxSpin);
+        }
+    } else if (warp < 8) {
+        // ---------------------------------------------------------- phi on Q
+        const int t = tid;
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
+            const int s = i % kAStages;
+            ok = mbar_wait(&m.full[s], (i / kAStages) & 1, max_spin);
+            phi_tile_256(stage(s), t, kC);
+            phi_tile_256(stage(s) + kTileBytes, t, kC);
+            fence_proxy_async_smem();
+            ok = named_bar_and(1, 256, ok);
+            if (!ok) break;
+            if (t == 0) mbar_arrive(&m.phi_done[s]);
+        }
+        if (!ok && t == 0) report_timeout(hdr);
+    } else {
+        // ---------------------------------------------------------- operand build + epilogue
+        const int t = tid - 256;                // 0..255
+        const int q4 = warp & 3, g = (warp - 8) >> 2;
+        const int row = 32 * q4 + lane;         // query row of the epilogue / operand row n
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+
+        // [S^T | z_hi | z_lo] for head h: S = sum of every run of head h (all CTAs).
+        auto build = [&](int h) {
+            const int64_t hb = (int64_t)h * part.nchunks, he = hb + part.nchunks;
+            // First CTA covering head h: largest c with begin(c) <= hb.
+            int c_lo = (int)((hb * part.grid) / part.T);
+            while (c_lo > 0 && part.begin(c_lo) > hb) --c_lo;
+            while (c_lo + 1 < part.grid && part.begin(c_lo + 1) <= hb) ++c_lo;
+            // Thread (row n, half g) sums column n of S over features c in [64g, 64g+64)
+            // and writes S^T[n][c] into sub-tile g; threads with n < 128 also own z[n] (g = 0).
+            float acc[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+            float zacc = 0.f;
+            for (int c2 = c_lo; c2 < part.grid && part.begin(c2) < he; ++c2) {
+                const int64_t b0 = part.begin(c2);
+                if (part.begin(c2 + 1) <= b0) continue;
+                const float* a = agg + ((int64_t)c2 * part.maxr + (h - b0 / part.nchunks)) * kE;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) acc[e] += a[(64 * g + e) * kD + row];
+                if (g == 0) zacc += a[kD * kD + row];
+            }
+            uint8_t* sub = bop + g * kBSub;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 v = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
+                                     pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
+                *reinterpret_cast<uint4*>(sub + sw128_offset(row, 8 * c)) = v;
+            }
+            if (g == 0) {
+                // z as two bf16 terms in rows 128 (hi) and 129 (lo), feature = row.
+                const uint32_t hi = pack_bf16(zacc, 0.f);
+                const uint32_t lo = pack_bf16(zacc - bf_lo(hi), 0.f);
+                uint8_t* zsub = bop + (row >> 6) * kBSub;
+                *reinterpret_cast<uint16_t*>(zsub + sw128_offset(kD, row & 63)) = (uint16_t)hi;
+                *reinterpret_cast<uint16_t*>(zsub + sw128_offset(kD + 1, row & 63)) = (uint16_t)lo;
+            }
+            fence_proxy_async_smem();
+            named_bar(2, 256);
+            if (t == 0) mbar_arrive(&m.b_ready);
+        };
+
+        pdl_wait();  // the state kernel's aggregates are complete and visible
+        bool ok = true;
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1;
+            const int64_t u = u0 + i;
+            const int h = (int)(u / part.nchunks), ch = (int)(u % part.nchunks);
+            // A new run: every MMA of the previous run has completed (its last
+            // output was read below), so the operand can be rebuilt.
+            if (i == 0 || ch == 0) build(h);
+            ok = mbar_wait(&m.o_full[b], (i >> 1) & 1, max_spin);
+            if (t == 0) tma_store_wait_read<0>();  // the staging tile is free again
+            named_bar(2, 256);
+            tc_fence_after();
+            const uint32_t to = tmem + kTmStride * b + lane_base;
+            float inv;
+            {
+                uint32_t rd[16];
+                tmem_ld16(to + kD, rd);
+                tmem_ld_wait();
+                inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
+            }
+            uint8_t* ot = ostage + g * kTileBytes;   // value columns [64g, 64g + 64)
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(to + 64 * g + 32 * c2, r0);
+                tmem_ld16(to + 64 * g + 32 * c2 + 16, r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t* rr = c < 2 ? r0 : r1;
+                    const int e0 = 8 * (c & 1);
+                    uint4 v = make_uint4(
+                        pack_bf16(__uint_as_float(rr[e0]) * inv, __uint_as_float(rr[e0 + 1]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 2]) * inv, __uint_as_float(rr[e0 + 3]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 4]) * inv, __uint_as_float(rr[e0 + 5]) * inv),
+                        pack_bf16(__uint_as_float(rr[e0 + 6]) * inv, __uint_as_float(rr[e0 + 7]) * inv));
+                    *reinterpret_cast<uint4*>(ot + sw128_offset(row, 32 * c2 + 8 * c)) = v;
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            ok = named_bar_and(2, 256, ok);
+            if (!ok) break;
+            if (t == 0) {
+                mbar_arrive(&m.o_free[b]);
+                tma_store_3d(&omap, ostage, 0, ch * kC, h);
+                tma_store_3d(&omap, ostage + kTileBytes, 64, ch * kC, h);
+                tma_store_commit();
+            }
+        }
+        if (!ok && t == 0) report_timeout(hdr);
+        if (t == 0) tma_store_wait_all<0>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 17) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+static_assert(kSSmem <= 232448, "state kernel shared memory exceeds 227 KB");
+static_assert(kASmem <= 232448, "apply kernel shared memory exceeds 227 KB");
+
+}  // namespace
+
+bool tc_noncausal_supported(int D, int M, la_dtype dt) {
+    return dt == LA_BF16 && D == kD && M == kD;
+}
+
+size_t tc_noncausal_workspace(int64_t BH, int N) {
+    Partition p = make_partition(BH, N, sm_count());
+    return sizeof(float) * (size_t)p.grid * p.maxr * kE;
+}
+
+cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
+                         float eps, void* ws_header, void* scratch, cudaStream_t st) {
+    Partition p = make_partition(BH, N, sm_count());
+    CUtensorMap qm, km, vm, om;
+    if (!encode_bhnd(&qm, q, BH, N, kD) || !encode_bhnd(&km, k, BH, N, kD) ||
+        !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
+        return cudaErrorInvalidValue;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
+    float* agg = reinterpret_cast<float*>(scratch);
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(nc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSSmem)))
+        return err;
+    if ((err = cudaFuncSetAttribute(nc_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kASmem)))
+        return err;
+    nc_state_kernel<<<p.grid, kSThreads, kSSmem, st>>>(km, vm, agg, p, N, hdr);
+    if ((err = cudaPeekAtLastError())) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kAThreads);
+    cfg.dynamicSmemBytes = kASmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, nc_apply_kernel, qm, om, (const float*)agg, p, eps, hdr);
+}
+
+}  // namespace la

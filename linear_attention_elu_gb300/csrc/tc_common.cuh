@@ -1,0 +1,170 @@
+// Helpers shared by the tensor-core kernels (causal and non-causal paths):
+// the persistent-CTA chunk partition, packed bf16 phi, barriers with uniform
+// abort decisions, constant operand tiles, programmatic-dependent-launch
+// controls and the host-side TMA descriptor encoding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tc_util.cuh"
+
+namespace la {
+namespace tcc {
+
+using namespace tc;
+
+constexpr int kC = 128;                        // tokens per chunk (one M = 128 row block)
+constexpr uint32_t kTileBytes = kC * 64 * 2;   // one bf16 [128 x 64] tile = 16 KB
+
+// The B*H*ceil(N/128) chunks in head-major order, cut into `grid` contiguous
+// ranges (one per persistent CTA). A range holds "runs": its chunks of one head.
+struct Partition {
+    int64_t T;      // total chunks = BH * nchunks
+    int nchunks;    // chunks per head
+    int grid;       // CTAs
+    int maxr;       // aggregate slots per CTA
+    __host__ __device__ int64_t begin(int c) const { return (int64_t)c * T / grid; }
+};
+
+inline Partition make_partition(int64_t BH, int N, int grid) {
+    Partition p;
+    p.nchunks = (N + kC - 1) / kC;
+    p.T = BH * p.nchunks;
+    p.grid = (int)(grid < p.T ? grid : p.T);
+    const int64_t len = (p.T + p.grid - 1) / p.grid;
+    p.maxr = (int)((len + p.nchunks - 1) / p.nchunks + 1);
+    return p;
+}
+
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+
+// phi(x) = max(x, 0) + min(2^(x log2 e), 1) on two packed bf16 values: equal
+// to x + 1 for x > 0 and e^x for x <= 0 (e^x >= 1 exactly when x >= 0).
+// x log2 e is formed as x*c_hi + x*c_lo with c_hi + c_lo = log2 e to about
+// 2^-17, rounded once to bf16; the power of two is the hardware ex2.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
+    constexpr uint32_t kLog2eHi = 0x3FB93FB9u;  // bf16(log2 e) = 1.4453125, twice
+    constexpr uint32_t kLog2eLo = 0xBB2CBB2Cu;  // bf16(log2 e - 1.4453125) = -0.00262451, twice
+    constexpr uint32_t kOne = 0x3F803F80u;
+    constexpr uint32_t kNegZero = 0x80008000u;
+    uint32_t lo, t, e, m, p, r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(x), "r"(kLog2eLo), "r"(kNegZero));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eHi), "r"(lo));
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(e), "r"(kOne));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(x), "r"(0u));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(m));
+    return r;
+}
+
+__device__ __forceinline__ uint4 phi8(uint4 u) {
+    return make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also ANDs `pred` over the participating threads, so that
+// every thread takes the same abort decision after a bounded wait.
+__device__ __forceinline__ bool named_bar_and(int id, int threads, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ void report_timeout(WsHeader* hdr) {
+    atomicCAS(&hdr->status, 0u, (uint32_t)LA_ERR_TIMEOUT);
+}
+
+// phi in place on the 128 x 64 bf16 tile rows (t >> 3) + 32 k, physical chunk
+// (t & 7), for a 256-thread group; rows >= zero_from are set to 0.
+__device__ __forceinline__ void phi_tile_256(uint8_t* tile, int t, int zero_from) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        v[k] = *reinterpret_cast<const uint4*>(tile + ((t >> 3) + 32 * k) * 128 + (t & 7) * 16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = (t >> 3) + 32 * k;
+        const uint4 o = r < zero_from ? phi8(v[k]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(tile + r * 128 + (t & 7) * 16) = o;
+    }
+}
+
+// The "ones" operand tile: 128 rows, logical column 0 = 1.0, the rest 0.
+__device__ __forceinline__ void init_ones_tile(uint8_t* tile, int t, int nthreads) {
+    for (int idx = t; idx < kC * 8; idx += nthreads) {
+        const int r = idx >> 3, pc = idx & 7;
+        const int logical = pc ^ (r & 7);
+        *reinterpret_cast<uint4*>(tile + r * 128 + pc * 16) =
+            make_uint4(logical == 0 ? 0x3F80u : 0u, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiled get_encoder() {
+    static EncodeTiled fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// [BH, N, D] bf16 viewed as 3-D (D, N, BH); box = 64 features x 128 tokens x 1 head.
+inline bool encode_bhnd(CUtensorMap* map, const void* ptr, int64_t BH, int N, int D) {
+    EncodeTiled enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+}  // namespace tcc
+}  // namespace la

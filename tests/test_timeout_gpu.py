@@ -44,3 +44,21 @@ def test_withheld_load_times_out_and_context_survives(la):
     got = to_f64(o)
     err = (np.abs(got - ref).max(-1) / np.abs(ref).max(-1)).max()
     assert err <= 2e-2
+
+
+def test_withheld_load_times_out_noncausal(la):
+    dev = torch.device("cuda")
+    q, k, v = make_qkv(1, 4, 700, 128, "bf16", seed=4)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws = la.workspace(la.LA_OP_NONCAUSAL, 1, 4, 700, 128, 128, torch.bfloat16, dev)
+    hdr = ws[:256].view(torch.int32)
+    hdr[MAX_SPIN_WORD] = 2000
+    hdr[HOLD_WORD] = 1
+    la.la_noncausal_fwd(qd, kd, vd, ws=ws)
+    assert la.la_query_status(ws) == la.LA_ERR_TIMEOUT
+    la.la_workspace_init(ws)
+    o = la.la_noncausal_fwd(qd, kd, vd, ws=ws)
+    assert la.la_query_status(ws) == 0
+    ref = oracle.recurrent(to_f64(q), to_f64(k), to_f64(v), False)
+    got = to_f64(o)
+    assert (np.abs(got - ref).max(-1) / np.abs(ref).max(-1)).max() <= 2e-2
