@@ -697,13 +697,10 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     float* agg = reinterpret_cast<float*>(scratch);
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(causal_state_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kStateSmem)))
-        return err;
-    if ((err = cudaFuncSetAttribute(causal_output_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem)))
-        return err;
+    static std::atomic<int> optin_causal_state_kernel[kMaxDevices];
+    if ((err = ensure_smem_optin(causal_state_kernel, (int)kStateSmem, optin_causal_state_kernel))) return err;
+    static std::atomic<int> optin_causal_output_kernel[kMaxDevices];
+    if ((err = ensure_smem_optin(causal_output_kernel, (int)kOutSmem, optin_causal_output_kernel))) return err;
     causal_state_kernel<<<p.grid, kStateThreads, kStateSmem, st>>>(km, vm, agg, p, N, hdr);
     if ((err = cudaPeekAtLastError())) return err;
     // The output kernel may start while the state kernel drains; it waits

@@ -512,12 +512,10 @@ cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, i
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     float* agg = reinterpret_cast<float*>(scratch);
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(nc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSSmem)))
-        return err;
-    if ((err = cudaFuncSetAttribute(nc_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kASmem)))
-        return err;
+    static std::atomic<int> optin_nc_state_kernel[kMaxDevices];
+    if ((err = ensure_smem_optin(nc_state_kernel, (int)kSSmem, optin_nc_state_kernel))) return err;
+    static std::atomic<int> optin_nc_apply_kernel[kMaxDevices];
+    if ((err = ensure_smem_optin(nc_apply_kernel, (int)kASmem, optin_nc_apply_kernel))) return err;
     nc_state_kernel<<<p.grid, kSThreads, kSSmem, st>>>(km, vm, agg, p, N, hdr);
     if ((err = cudaPeekAtLastError())) return err;
     cudaLaunchConfig_t cfg = {};

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "tc_util.cuh"
 
@@ -158,12 +160,32 @@ inline bool encode_bhnd(CUtensorMap* map, const void* ptr, int64_t BH, int N, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 128;
+
+// SM count of the current device (cached per device; host-only).
 inline int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return 148;
+    cache[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+// Opts `kernel` in to `bytes` of dynamic shared memory once per device (the
+// setting is per function and device; repeating it costs host time per call).
+template <typename Kernel>
+inline cudaError_t ensure_smem_optin(Kernel kernel, int bytes, std::atomic<int>* done) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(1, std::memory_order_release);
+    return err;
 }
 
 }  // namespace tcc
