@@ -33,13 +33,13 @@ struct WsHeader {
     uint32_t epoch;      // launch generation for flag-based cross-CTA waits
     uint32_t ticket;     // dynamic work-item counter of the running launch
     uint32_t done;       // CTAs finished in the running launch
-    uint32_t max_spin;   // iteration limit of every bounded wait
+    uint32_t max_spin;   // limit of every bounded wait, in microseconds
     uint32_t hold_item;  // test hook: work item + 1 whose publication is withheld
     uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
-constexpr uint32_t kDefaultMaxSpin = 1u << 22;  // ~0.5 s with 100 ns backoff
+constexpr uint32_t kDefaultMaxSpin = 2000000;   // 2 s
 
 __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
     atomicCAS(&h->status, 0u, code);

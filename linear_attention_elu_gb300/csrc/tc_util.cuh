@@ -49,29 +49,38 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One bounded hardware wait: the thread is suspended until the phase with the
+// given parity completes or about `hint_ns` nanoseconds pass. Returns whether
+// the phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns = 10000) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. try_wait suspends the
-// thread until the phase completes or a hardware time slice ends; between
-// polls the loop sleeps briefly. Gives up after `max_spin` polls and returns
-// false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_spin) {
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// `limit_us` microseconds of wall time; returns false if it did not.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit_us) {
     if (mbar_try_wait(bar, parity)) return true;
-    for (uint32_t i = 0; i < max_spin; ++i) {
-        __nanosleep(64);
+    const uint64_t t0 = global_ns();
+    const uint64_t limit = (uint64_t)limit_us * 1000u;
+    while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit) return mbar_try_wait(bar, parity, 0);
     }
-    return false;
 }
 
 // ------------------------------------------------------------------ fences

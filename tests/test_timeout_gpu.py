@@ -5,7 +5,7 @@ usable.
 The workspace header carries the wait limit (max_spin) and a test hook
 (hold_item): when hold_item is set, the TMA producer of the tensor-core causal
 path never issues its first load, so the consumers' waits on that load cannot
-complete. Each wait gives up after max_spin polls, the kernel records
+complete. Each wait gives up after max_spin microseconds, the kernel records
 LA_ERR_TIMEOUT in the header and returns; la_query_status reports it.
 """
 import numpy as np
@@ -32,7 +32,7 @@ def test_withheld_load_times_out_and_context_survives(la):
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     ws = la.workspace(la.LA_OP_CAUSAL, 2, 2, 1000, 64, 64, torch.bfloat16, dev)
     hdr = ws[:256].view(torch.int32)
-    hdr[MAX_SPIN_WORD] = 2000
+    hdr[MAX_SPIN_WORD] = 2000  # 2 ms
     hdr[HOLD_WORD] = 1
     la.la_causal_fwd(qd, kd, vd, ws=ws)
     assert la.la_query_status(ws) == la.LA_ERR_TIMEOUT
@@ -52,7 +52,7 @@ def test_withheld_load_times_out_noncausal(la):
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     ws = la.workspace(la.LA_OP_NONCAUSAL, 1, 4, 700, 128, 128, torch.bfloat16, dev)
     hdr = ws[:256].view(torch.int32)
-    hdr[MAX_SPIN_WORD] = 2000
+    hdr[MAX_SPIN_WORD] = 2000  # 2 ms
     hdr[HOLD_WORD] = 1
     la.la_noncausal_fwd(qd, kd, vd, ws=ws)
     assert la.la_query_status(ws) == la.LA_ERR_TIMEOUT
