@@ -93,7 +93,12 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
 la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
                           int* launches);
 
-/* Zero-fills the workspace header and sets the default wait limit (async on stream). */
+/*
+ * Prepares the workspace header (its first 4096 bytes): clears the status
+ * word and the cross-CTA flags and sets the default wait limit (async on
+ * stream). Needed once per workspace, and again after a call was abandoned
+ * mid-flight (a killed process, a reset device).
+ */
 la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
@@ -131,9 +136,10 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
  *    initialises its header on `stream`; make that first call before any
  *    stream capture.
  *  - Shapes whose scratch would exceed 16 MiB return LA_ERR_WORKSPACE and
- *    launch nothing. For bf16 with Dk = Dv = 64 on a 152-SM GPU every shape
- *    with B*H <= 760 fits, whatever N; the fp32 path keeps one state per
- *    64-token chunk and fits B*H*ceil(N/64) <= 1008 at Dk = Dv = 64.
+ *    launch nothing. bf16 with Dk = Dv = 64 needs two fp32 state sums per
+ *    CTA (about 5 MB on a 152-SM GPU) whatever the shape, so it always fits.
+ *    The other paths keep one fp32 state per 64-token chunk: at
+ *    Dk = Dv = 64 they fit B*H*ceil(N/64) <= 1008.
  *  - All calls share the one array, which keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, or concurrent host
  *    threads without ordering) race on it and must be serialised by the caller.

@@ -59,11 +59,12 @@ def test_noalloc_matches_workspace_entry_point(B, H, N, dtype):
 
 
 def test_noalloc_rejects_shapes_beyond_its_capacity():
-    # Thousands of short bf16 heads need more scratch than the fixed array holds:
-    # the call must refuse before touching any pointer (these are never dereferenced).
+    # Paths that keep one state per chunk need more scratch than the fixed array
+    # holds at these shapes: the call must refuse before touching any pointer
+    # (these are never dereferenced).
     _, f = _fn()
     fake = 1 << 20
-    rc = f(fake, fake, fake, fake, 64, 1000, 128, 64, 64, LA_BF16, 1e-6, None, None, None)
+    rc = f(fake, fake, fake, fake, 64, 1000, 128, 32, 32, LA_BF16, 1e-6, None, None, None)
     assert rc == LA_ERR_WORKSPACE
     rc = f(fake, fake, fake, fake, 8, 8, 65536, 64, 64, LA_F32, 1e-6, None, None, None)
     assert rc == LA_ERR_WORKSPACE
