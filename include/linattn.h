@@ -94,10 +94,14 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
                           int* launches);
 
 /*
- * Prepares the workspace header (its first 4096 bytes): clears the status
- * word and the cross-CTA flags and sets the default wait limit (async on
- * stream). Needed once per workspace, and again after a call was abandoned
- * mid-flight (a killed process, a reset device).
+ * Prepares a workspace (async on stream): zero-fills all `workspace_bytes`
+ * bytes, then sets the header (its first 256 bytes) to no error, launch
+ * counters at zero and the default wait limit. Needed once per workspace, and
+ * again after a call was abandoned mid-flight (a killed process, a reset
+ * device). Calls then keep the workspace consistent: the causal tensor-core
+ * path publishes per-CTA sums in the body as words tagged with a launch
+ * counter kept in the header, so the body must not be written by anything
+ * else between init and the calls that use it.
  */
 la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t stream);
 
@@ -136,8 +140,8 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
  *    initialises its header on `stream`; make that first call before any
  *    stream capture.
  *  - Shapes whose scratch would exceed 16 MiB return LA_ERR_WORKSPACE and
- *    launch nothing. bf16 with Dk = Dv = 64 needs two fp32 state sums per
- *    CTA (about 5 MB on a 152-SM GPU) whatever the shape, so it always fits.
+ *    launch nothing. bf16 with Dk = Dv = 64 needs two tagged state sums per
+ *    CTA (about 10 MB on a 152-SM GPU) whatever the shape, so it always fits.
  *    The other paths keep one fp32 state per 64-token chunk: at
  *    Dk = Dv = 64 they fit B*H*ceil(N/64) <= 1008.
  *  - All calls share the one array, which keeps the last call's contents:

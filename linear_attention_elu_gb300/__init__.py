@@ -136,7 +136,7 @@ def la_workspace_init(ws, stream=None):
 def workspace(op, B, H, N, Dk, Dv, dtype, device=None, stream=None):
     """Allocates (through PyTorch) and initialises a workspace for `op` at this shape."""
     n = la_workspace_size(op, B, H, N, Dk, Dv, dtype)
-    ws = torch.empty(max(n, 4096), dtype=torch.uint8, device=device or "cuda")
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
     return la_workspace_init(ws, stream)
 
 

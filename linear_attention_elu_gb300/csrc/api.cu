@@ -60,7 +60,7 @@ la_status check_workspace(void* ws, size_t have, size_t need) {
 
 la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
-__global__ void init_header_kernel(WsHeader* h) { la::init_header(h, threadIdx.x, blockDim.x); }
+__global__ void init_header_kernel(WsHeader* h) { la::init_header(h); }
 
 }  // namespace
 
@@ -121,7 +121,11 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
 la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t stream) {
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < kHeaderBytes)
         return LA_ERR_WORKSPACE;
-    init_header_kernel<<<1, 128, 0, (cudaStream_t)stream>>>((WsHeader*)workspace);
+    // The body is cleared too: kernels that publish tagged words across CTAs
+    // trust a word only when it carries the current launch's tag.
+    cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return LA_ERR_CUDA;
+    init_header_kernel<<<1, 1, 0, (cudaStream_t)stream>>>((WsHeader*)workspace);
     return from_cuda(cudaPeekAtLastError());
 }
 

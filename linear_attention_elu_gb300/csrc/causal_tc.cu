@@ -20,20 +20,19 @@
 // head-major sequence cut into gridDim.x contiguous ranges, one per CTA. A
 // range holds "runs" (its chunks of one head). Each CTA
 //  1. sums [dS | dz] = phi(K)^T [V | 1] over its last run when that run's head
-//     continues into the next range, and publishes the sum (fp32, workspace)
-//     behind a flag;
+//     continues into the next range, and publishes the sum (fp32) in the
+//     workspace as tagged words (value and launch tag in one 64-bit store);
 //  2. if its first run continues a head from earlier ranges, looks back over
-//     the flags of the ranges to its left and adds their published sums (or
-//     stops at the first range that already published its inclusive prefix):
-//     the exclusive prefix over segments, as in the parallel scan of the same
-//     blog, section 7.7, in fp32 (decoupled look-back);
+//     the ranges to its left and adds their published sums (or stops at the
+//     first range that already published its inclusive prefix): the exclusive
+//     prefix over segments, as in the parallel scan of the same blog, section
+//     7.7, in fp32 (decoupled look-back);
 //  3. runs the chunk loop above over its whole range with the running state
-//     [S | z] in TMEM (fp32, accumulated by the tensor core), writing each
-//     chunk's S_{c-1}, z_{c-1} as bf16 rows right behind the K tile in shared
-//     memory, where they form one MMA operand with phi(K).
+//     [S | z] in registers (fp32), writing each chunk's S_{c-1}, z_{c-1} as bf16
+//     rows behind the Q, K, V tiles of its stage in shared memory.
 // The last run's K and V are read twice (steps 1 and 3); the second read is
-// expected to hit L2. Flags carry the launch epoch from the workspace header;
-// the last CTA to finish advances it.
+// expected to hit L2. Tags are the launch epoch from the workspace header plus
+// one; the last CTA to finish advances the epoch.
 //
 // Data movement: TMA 3-D tiles (64 features x 128 tokens x 1 head, 128-byte
 // swizzle) into shared memory; phi is applied in place in shared memory with
@@ -129,15 +128,22 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+// Published sums are tagged words: bits of the fp32 value in the low half, the
+// launch tag (epoch + 1) in the high half, stored and loaded as single 64-bit
+// accesses, so a reader that sees the tag also sees the value: no fence or flag.
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
 }
+
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
 // Writes 16 fp32 values as bf16 into row `row`, columns c0..c0+15 of a swizzled tile.
 __device__ __forceinline__ void put_row16(uint8_t* tile, int row, int c0, const float* f) {
@@ -173,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
-                    const __grid_constant__ CUtensorMap omap, float* __restrict__ agg,
-                    float* __restrict__ incl, float* __restrict__ S_out,
+                    const __grid_constant__ CUtensorMap omap, uint64_t* __restrict__ agg,
+                    uint64_t* __restrict__ incl, float* __restrict__ S_out,
                     float* __restrict__ z_out, Partition part, int N, float eps, WsHeader* hdr) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -427,9 +433,11 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
         const int v = 32 * q4 + lane;
         const uint32_t tst = tmem + kTmState + lane_base + 32 * hh;
         const uint32_t epoch1 = *reinterpret_cast<volatile uint32_t*>(&hdr->epoch) + 1u;
-        float* my_agg = agg + (int64_t)cta * kE;
+        uint64_t* my_agg = agg + (int64_t)cta * kE;
+        float* sum_s = reinterpret_cast<float*>(base + kOffSum);
         bool ok = true;
-        // Step 1: publish the last run's sum (fp32).
+        // Step 1: publish the last run's sum (fp32, tagged); keep a copy in shared
+        // memory for this range's inclusive prefix.
         if (nA > 0) {
             ok = mbar_wait(&m.a_done, 0, max_spin);
             tc_fence_after();
@@ -440,17 +448,17 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             tc_fence_before();
             if (v <= kD) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) my_agg[sum_idx(v, 32 * hh + e)] = __uint_as_float(r[e >> 4][e & 15]);
-            }
-            // Publication: the CTA barrier orders every thread's stores before
-            // thread 0's release of the flag (release is cumulative).
-            ok = named_bar_and(kBarEpi, kEpiThreads, ok);
-            if (ok && t == 0) {
-                __threadfence();
-                st_release(&hdr->aflag[cta], epoch1);
+                for (int e = 0; e < 32; ++e) {
+                    const int idx = sum_idx(v, 32 * hh + e);
+                    const float x = __uint_as_float(r[e >> 4][e & 15]);
+                    st_tagged(my_agg + idx, x, epoch1);
+                    sum_s[idx] = x;
+                }
             }
         }
-        // Step 2: look back over the ranges to the left for the head's earlier part.
+        // Step 2: look back over the ranges to the left for the head's earlier
+        // part: a range's inclusive prefix ends the walk, else its sum is added and
+        // the walk goes on until the range that holds the head's start.
         int stop = cta, stop_incl = 0;
         if (ok && use_prefix) {
             if (t == 0) {
@@ -458,13 +466,13 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 bool found = false;
                 const uint64_t t0 = global_ns();
                 while (!found) {
-                    const uint32_t pf = ld_acquire(&hdr->pflag[r2]);
-                    const uint32_t af = ld_acquire(&hdr->aflag[r2]);
-                    if (pf == epoch1) {
+                    const uint64_t pw = ld_tagged(incl + (int64_t)r2 * kE);
+                    const uint64_t aw = ld_tagged(agg + (int64_t)r2 * kE);
+                    if (tag_of(pw) == epoch1) {
                         stop = r2;
                         stop_incl = 1;
                         found = true;
-                    } else if (af == epoch1) {
+                    } else if (tag_of(aw) == epoch1) {
                         if (part.begin(r2) <= hb) {
                             stop = r2;
                             found = true;
@@ -478,41 +486,52 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 m.walk_stop = found ? stop : -1;
                 m.walk_incl = stop_incl;
             }
-            named_bar(kBarEpi, kEpiThreads);     // thread 0 acquired the flags it used
+        }
+        // Seed: state before the range = prefix (or zero) for chunk 0's rows and
+        // the state role; inclusive prefix for ranges to the right.
+        if (ok && nA > 0) ok = mbar_wait(&m.a_done, 0, max_spin);   // stage memory is free
+        ok = named_bar_and(kBarEpi, kEpiThreads, ok);
+        if (ok && use_prefix) {
             stop = m.walk_stop;
             stop_incl = m.walk_incl;
             ok = stop >= 0;
             if (!ok) stop = cta;
         }
-        // Seed: state before the range = prefix (or zero) into the TMEM running
-        // state and chunk 0's rows; inclusive prefix for ranges to the right.
-        if (ok && nA > 0) ok = mbar_wait(&m.a_done, 0, max_spin);   // stage memory is free
-        ok = named_bar_and(kBarEpi, kEpiThreads, ok);
         if (ok) {
             // Prefix sum in fp32, element idx = t + 256 k, staged in shared memory.
-            float* sum_s = reinterpret_cast<float*>(base + kOffSum);
+            // Every word is checked for this launch's tag (re-read until it holds it).
             constexpr int kPer = (kE + kEpiThreads - 1) / kEpiThreads;   // 17
-            float acc[kPer], own[kPer];
+            float acc[kPer];
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                const int idx = t + kEpiThreads * k;
-                acc[k] = 0.f;
-                own[k] = (publish_P && idx < kE) ? __ldcg(my_agg + idx) : 0.f;   // written by this CTA
-            }
-            for (int r2 = stop; r2 < cta; ++r2) {
-                const float* src = (r2 == stop && stop_incl ? incl : agg) + (int64_t)r2 * kE;
+            for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+            const uint64_t t0 = global_ns();
+            for (int r2 = stop; r2 < cta && ok; ++r2) {
+                const uint64_t* src = (r2 == stop && stop_incl ? incl : agg) + (int64_t)r2 * kE;
+                uint64_t w[kPer];
 #pragma unroll
                 for (int k = 0; k < kPer; ++k) {
                     const int idx = t + kEpiThreads * k;
-                    if (idx < kE) acc[k] += __ldcg(src + idx);
+                    w[k] = idx < kE ? ld_tagged(src + idx) : ((uint64_t)epoch1 << 32);
+                }
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int idx = t + kEpiThreads * k;
+                    while (tag_of(w[k]) != epoch1) {
+                        if (global_ns() - t0 > (uint64_t)max_spin * 1000u) {
+                            ok = false;
+                            break;
+                        }
+                        w[k] = ld_tagged(src + idx);
+                    }
+                    acc[k] += value_of(w[k]);
                 }
             }
 #pragma unroll
             for (int k = 0; k < kPer; ++k) {
                 const int idx = t + kEpiThreads * k;
                 if (idx < kE) {
+                    if (publish_P) st_tagged(incl + (int64_t)cta * kE + idx, acc[k] + sum_s[idx], epoch1);
                     sum_s[idx] = acc[k];
-                    if (publish_P) incl[(int64_t)cta * kE + idx] = acc[k] + own[k];
                 }
             }
             // z padding rows 2-15 of every stage (the (3) operand's last 14 rows).
@@ -520,7 +539,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 const int s = idx / 112, r = idx % 112;
                 *reinterpret_cast<uint4*>(stage(s) + kStZ + 256 + r * 16) = make_uint4(0, 0, 0, 0);
             }
-            named_bar(kBarEpi, kEpiThreads);
+            ok = named_bar_and(kBarEpi, kEpiThreads, ok);
             // This thread's TMEM lane v, columns 32 hh .. 32 hh + 31.
             uint8_t* st0 = stage(0) + kStS;
 #pragma unroll
@@ -533,13 +552,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             fence_proxy_async_smem();
             named_bar(kBarEpi, kEpiThreads);
-            if (t == 0) {
-                mbar_arrive(&m.snap_ready[0]);
-                if (publish_P) {
-                    __threadfence();
-                    st_release(&hdr->pflag[cta], epoch1);
-                }
-            }
+            if (ok && t == 0) mbar_arrive(&m.snap_ready[0]);
         }
         if (hh == 0) {
             // ------------------------------------------------------ mask (warps 8-11)
@@ -727,16 +740,17 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
 
 static_assert(kSmem <= 232448, "shared memory exceeds 227 KB");
 
-int grid_cap() { return sm_count() < kMaxFlags ? sm_count() : kMaxFlags; }
+int grid_cap() { return sm_count(); }
 
 }  // namespace
 
 bool tc_causal_supported(int D, int M, la_dtype dt) { return dt == LA_BF16 && D == 64 && M == 64; }
 
-// Workspace after the header: per CTA one published sum and one inclusive prefix (fp32).
+// Workspace after the header: per CTA one published sum and one inclusive prefix
+// (tagged 64-bit words).
 size_t tc_causal_workspace(int64_t BH, int N) {
     Partition p = make_partition(BH, N, grid_cap());
-    return 2 * sizeof(float) * (size_t)p.grid * kE;
+    return 2 * sizeof(uint64_t) * (size_t)p.grid * kE;
 }
 
 int tc_causal_launches() { return 1; }
@@ -746,8 +760,8 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
                       cudaStream_t st) {
     Partition p = make_partition(BH, N, grid_cap());
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
-    float* agg = reinterpret_cast<float*>(scratch);
-    float* incl = agg + (size_t)p.grid * kE;
+    uint64_t* agg = reinterpret_cast<uint64_t*>(scratch);
+    uint64_t* incl = agg + (size_t)p.grid * kE;
     CUtensorMap qm, km, vm, om;
     if (!encode_bhnd(&qm, q, BH, N, kD) || !encode_bhnd(&km, k, BH, N, kD) ||
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))

@@ -27,23 +27,17 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
-// Cross-CTA publication flags kept in the workspace header (one per CTA of a
-// persistent launch, so launches use at most this many CTAs).
-constexpr int kMaxFlags = 480;
-
-// Workspace header (first 4096 bytes of every workspace).
+// Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
     uint32_t status;     // 0 = ok, else an la_status code set by a kernel
-    uint32_t epoch;      // launches of flag-publishing kernels completed so far
+    uint32_t epoch;      // launches of cross-CTA publishing kernels completed so far
     uint32_t ticket;     // reserved
-    uint32_t done;       // CTAs finished in the running flag-publishing launch
+    uint32_t done;       // CTAs finished in the running cross-CTA publishing launch
     uint32_t max_spin;   // limit of every bounded wait, in microseconds
     uint32_t hold_item;  // test hook: when set, input loads are withheld
     uint32_t pad[58];
-    uint32_t aflag[kMaxFlags];  // CTA c published its aggregate: epoch + 1
-    uint32_t pflag[kMaxFlags];  // CTA c published its inclusive prefix: epoch + 1
 };
-static_assert(sizeof(WsHeader) == 4096, "workspace header is 4096 bytes");
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 constexpr uint32_t kDefaultMaxSpin = 2000000;   // 2 s
 
@@ -51,20 +45,14 @@ __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
     atomicCAS(&h->status, 0u, code);
 }
 
-// Header defaults: no error, default wait limit, test hook off, flags clear.
-__device__ __forceinline__ void init_header(WsHeader* h, int t, int nthreads) {
-    if (t == 0) {
-        h->status = 0;
-        h->epoch = 0;
-        h->ticket = 0;
-        h->done = 0;
-        h->max_spin = kDefaultMaxSpin;
-        h->hold_item = 0;
-    }
-    for (int i = t; i < kMaxFlags; i += nthreads) {
-        h->aflag[i] = 0;
-        h->pflag[i] = 0;
-    }
+// Header defaults: no error, default wait limit, test hook off.
+__device__ __forceinline__ void init_header(WsHeader* h) {
+    h->status = 0;
+    h->epoch = 0;
+    h->ticket = 0;
+    h->done = 0;
+    h->max_spin = kDefaultMaxSpin;
+    h->hold_item = 0;
 }
 
 }  // namespace la

@@ -30,7 +30,7 @@ void* g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device; 
 
 // Header defaults: no error, default wait limit, test hook off.
 __global__ void noalloc_init_header() {
-    la::init_header(reinterpret_cast<la::WsHeader*>(g_scratch), threadIdx.x, blockDim.x);
+    la::init_header(reinterpret_cast<la::WsHeader*>(g_scratch));
 }
 
 // First use on a device: resolve the array's device address (with that device
@@ -42,7 +42,7 @@ la_status scratch_for_current_device(cudaStream_t st, void** out) {
     if (!g_scratch_addr[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || !ptr) return LA_ERR_CUDA;
-        noalloc_init_header<<<1, 128, 0, st>>>();
+        noalloc_init_header<<<1, 1, 0, st>>>();
         if (cudaPeekAtLastError() != cudaSuccess) return LA_ERR_CUDA;
         g_scratch_addr[dev] = ptr;
     }
