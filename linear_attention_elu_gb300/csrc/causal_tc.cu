@@ -185,8 +185,12 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     __shared__ Misc m;
-    const uint32_t max_spin = hdr->max_spin;
-    const bool hold = hdr->hold_item != 0;
+    // Launched as a programmatic dependent of the previous kernel in the stream:
+    // the set-up below touches no global memory; griddepcontrol.wait then orders
+    // everything after it behind that kernel's completion.
+    pdl_launch_dependents();
+    uint32_t max_spin = 0;
+    bool hold = false;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
     const int nchunks = part.nchunks;
@@ -252,6 +256,9 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    max_spin = hdr->max_spin;
+    hold = hdr->hold_item != 0;
     const uint32_t tmem = m.tmem_slot;
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
@@ -599,47 +606,48 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             if (!ok && tm == 0) report_timeout(hdr);
         } else {
             // ------------------------------------------------------ output (warps 12-15)
+            // Thread = query row v of its lane quarter. The TMEM buffer is released
+            // as soon as num and den are in registers (scaled and packed to bf16).
             const int to_t = t - 128;                     // 0..127
             for (int j = 0; j < nch && ok; ++j) {
                 const int bj = j & 1;
                 const int64_t u = u0 + j;
                 const int h = (int)(u / nchunks), ch = (int)(u % nchunks);
                 ok = mbar_wait(&m.o_full[bj], (j >> 1) & 1, max_spin);
-                if (to_t == 0) tma_store_wait_read<0>();  // the staging tile is free again
-                named_bar(kBarPair + 1, 128);
                 tc_fence_after();
                 const uint32_t to = tmem + kTmBuf * bj + kTmNum + lane_base;
-                uint32_t rd[16], r0[16], r1[16];
-                tmem_ld16(to + 64, rd);
-                tmem_ld16(to, r0);
-                tmem_ld16(to + 16, r1);
-                tmem_ld_wait();
-                const float inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    if (c2 == 1) {
-                        tmem_ld16(to + 32, r0);
-                        tmem_ld16(to + 48, r1);
-                        tmem_ld_wait();
-                    }
+                uint32_t o[32];
+                {
+                    uint32_t rd[16];
+                    tmem_ld16(to + 64, rd);
+                    tmem_ld_wait();
+                    const float inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t* rr = c < 2 ? r0 : r1;
-                        const int e0 = 8 * (c & 1);
-                        uint4 o = make_uint4(
-                            pack_bf16(__uint_as_float(rr[e0]) * inv, __uint_as_float(rr[e0 + 1]) * inv),
-                            pack_bf16(__uint_as_float(rr[e0 + 2]) * inv, __uint_as_float(rr[e0 + 3]) * inv),
-                            pack_bf16(__uint_as_float(rr[e0 + 4]) * inv, __uint_as_float(rr[e0 + 5]) * inv),
-                            pack_bf16(__uint_as_float(rr[e0 + 6]) * inv, __uint_as_float(rr[e0 + 7]) * inv));
-                        *reinterpret_cast<uint4*>(ostage + sw128_offset(v, 32 * c2 + 8 * c)) = o;
+                        uint32_t r[16];
+                        tmem_ld16(to + 16 * c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[8 * c + e] = pack_bf16(__uint_as_float(r[2 * e]) * inv,
+                                                     __uint_as_float(r[2 * e + 1]) * inv);
                     }
                 }
                 tc_fence_before();
-                fence_proxy_async_smem();
                 ok = named_bar_and(kBarPair + 1, 128, ok);
                 if (!ok) break;
                 if (to_t == 0) {
                     mbar_arrive(&m.o_free[bj]);
+                    tma_store_wait_read<0>();             // the staging tile is free again
+                }
+                named_bar(kBarPair + 1, 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(ostage + sw128_offset(v, 8 * c)) =
+                        make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                fence_proxy_async_smem();
+                named_bar(kBarPair + 1, 128);
+                if (to_t == 0) {
                     tma_store_3d(&omap, ostage, 0, ch * kC, h);
                     tma_store_commit();
                 }
@@ -769,9 +777,21 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
     cudaError_t err;
     static std::atomic<int> optin[kMaxDevices];
     if ((err = ensure_smem_optin(causal_fused_kernel, (int)kSmem, optin))) return err;
-    causal_fused_kernel<<<p.grid, kThreads, kSmem, st>>>(qm, km, vm, om, agg, incl, S_out, z_out,
-                                                         p, N, eps, hdr);
-    return cudaPeekAtLastError();
+    // Programmatic stream serialization: the next call's CTAs may be scheduled on
+    // SMs as this launch's CTAs finish and run their set-up; the kernel waits
+    // (griddepcontrol.wait) before its first global-memory access.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, causal_fused_kernel, qm, km, vm, om, agg, incl, S_out, z_out,
+                              p, N, eps, hdr);
 }
 
 }  // namespace la
