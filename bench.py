@@ -55,6 +55,26 @@ def dist_env():
     return rank, world, local
 
 
+def replica_seed(rank, r):
+    """Seed of input set r on rank `rank`: every rank draws its own batch (weak scaling)."""
+    return rank * 1000 + r
+
+
+def job_ms(ms, dist, device):
+    """Whole-job time of a timed region: the maximum over ranks (no-op on one rank)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Aggregate throughput: the units all ranks processed over the whole-job time."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -302,7 +322,7 @@ def main():
     R = max(2, -(-3 * L2_BYTES // per_set) + 1)
     sets = []
     for r in range(R):
-        q, k, v = make_workload(w, seed=rank * 1000 + r)
+        q, k, v = make_workload(w, seed=replica_seed(rank, r))
         sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(v, device=dev)))
     ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, sets[0][0].dtype, dev)
     stream = torch.cuda.current_stream(dev)
@@ -353,18 +373,15 @@ def main():
         g_timed.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
+    ms = job_ms(ev0.elapsed_time(ev1), dist, dev)
     if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     status = la.la_query_status(ws)
     if status != 0:
         raise RuntimeError(f"device status after timed region: {la.la_status_string(status)}")
     ms_per_step = ms / args.steps
     tokens = w.tokens * world
-    value = tokens / (ms_per_step * 1e-3)
+    value = job_rate(w.tokens, world, ms_per_step)
 
     # Per-call device time: events around each replay (one call each).
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -388,7 +405,7 @@ def main():
     eager_ms = ea.elapsed_time(eb) / args.steps
 
     # End to end: pinned host inputs -> device, forward, result -> pinned host.
-    hq, hk, hv = (t.cpu().pin_memory() for t in make_workload(w, seed=rank * 1000 + 77))
+    hq, hk, hv = (t.cpu().pin_memory() for t in make_workload(w, seed=replica_seed(rank, 77)))
     ho = torch.empty_like(hv).pin_memory()
     dq, dk, dv, do = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, ho))
 
@@ -411,11 +428,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = job_ms(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size()
     del sets, graphs, g_warm, g_timed
