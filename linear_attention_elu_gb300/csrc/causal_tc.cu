@@ -465,31 +465,42 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         // Step 2: look back over the ranges to the left for the head's earlier
         // part: a range's inclusive prefix ends the walk, else its sum is added and
-        // the walk goes on until the range that holds the head's start.
+        // the walk goes on until the range that holds the head's start. The first
+        // epi warp polls 32 ranges at once (lane l: range cta - 1 - l - 32 w).
         int stop = cta, stop_incl = 0;
-        if (ok && use_prefix) {
-            if (t == 0) {
-                int r2 = cta - 1;
-                bool found = false;
-                const uint64_t t0 = global_ns();
-                while (!found) {
+        if (ok && use_prefix && warp == kEpiW0) {
+            bool found = false;
+            const uint64_t t0 = global_ns();
+            int win = cta - 1;                     // range polled by lane 0
+            while (!found) {
+                const int r2 = win - lane;
+                bool isP = false, isA = false, isH = false;
+                if (r2 >= 0) {
                     const uint64_t pw = ld_tagged(incl + (int64_t)r2 * kE);
                     const uint64_t aw = ld_tagged(agg + (int64_t)r2 * kE);
-                    if (tag_of(pw) == epoch1) {
-                        stop = r2;
-                        stop_incl = 1;
-                        found = true;
-                    } else if (tag_of(aw) == epoch1) {
-                        if (part.begin(r2) <= hb) {
-                            stop = r2;
-                            found = true;
-                        } else {
-                            --r2;
-                        }
-                    } else if (global_ns() - t0 > (uint64_t)max_spin * 1000u) {
-                        break;
-                    }
+                    isP = tag_of(pw) == epoch1;
+                    isA = tag_of(aw) == epoch1;
+                    isH = part.begin(r2) <= hb;
                 }
+                const uint32_t endm = __ballot_sync(0xffffffffu, isP || (isA && isH));
+                const uint32_t am = __ballot_sync(0xffffffffu, isA);
+                const uint32_t pm = __ballot_sync(0xffffffffu, isP);
+                if (endm != 0u) {
+                    const int e = __ffs(endm) - 1;
+                    const uint32_t before = (1u << e) - 1u;     // lanes whose sums are added
+                    if ((am & before) == before) {
+                        stop = win - e;
+                        stop_incl = (pm >> e) & 1u;
+                        found = true;
+                    }
+                } else if (am == 0xffffffffu) {
+                    win -= 32;                     // all 32 published, none ends the walk
+                }
+                // One lane's clock decides, so that the whole warp leaves together.
+                const int late = __shfl_sync(0xffffffffu, (int)(global_ns() - t0 > (uint64_t)max_spin * 1000u), 0);
+                if (!found && late) break;
+            }
+            if (lane == 0) {
                 m.walk_stop = found ? stop : -1;
                 m.walk_incl = stop_incl;
             }
