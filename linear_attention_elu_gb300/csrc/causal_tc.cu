@@ -424,8 +424,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             const int s = i % kStages;
             const int ch = (int)((u0 + i) % nchunks);
             ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
-            phi_tile_256(stage(s) + kStK, t, min(kC, N - ch * kC));
-            phi_tile_256(stage(s) + kStQ, t, kC);
+            phi_tiles2_256(stage(s) + kStK, min(kC, N - ch * kC), stage(s) + kStQ, kC, t);
             fence_proxy_async_smem();
             ok = named_bar_and(kBarPhi, kPhiThreads, ok);
             if (ok && t == 0) mbar_arrive(&m.phi_done[s]);
@@ -627,22 +626,26 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 ok = mbar_wait(&m.o_full[bj], (j >> 1) & 1, max_spin);
                 tc_fence_after();
                 const uint32_t to = tmem + kTmBuf * bj + kTmNum + lane_base;
+                // Two TMEM round trips: den (two columns) with num 0..31, then num 32..63.
                 uint32_t o[32];
                 {
-                    uint32_t rd[16];
-                    tmem_ld16(to + 64, rd);
+                    uint32_t rd[2], r[2][16];
+                    tmem_ld2(to + 64, rd);
+                    tmem_ld16(to, r[0]);
+                    tmem_ld16(to + 16, r[1]);
                     tmem_ld_wait();
                     const float inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[16];
-                        tmem_ld16(to + 16 * c, r);
-                        tmem_ld_wait();
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = pack_bf16(__uint_as_float(r[e >> 3][2 * (e & 7)]) * inv,
+                                         __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) * inv);
+                    tmem_ld16(to + 32, r[0]);
+                    tmem_ld16(to + 48, r[1]);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            o[8 * c + e] = pack_bf16(__uint_as_float(r[2 * e]) * inv,
-                                                     __uint_as_float(r[2 * e + 1]) * inv);
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        o[16 + e] = pack_bf16(__uint_as_float(r[e >> 3][2 * (e & 7)]) * inv,
+                                              __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) * inv);
                 }
                 tc_fence_before();
                 ok = named_bar_and(kBarPair + 1, 128, ok);
@@ -706,14 +709,20 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             tc_fence_before();
             if (head_last) {
+                // Final head state: through the (now unused) look-back sum buffer in
+                // shared memory, then copied out row-major by all state threads
+                // (direct per-element global stores cost registers in this loop).
+                float* sum_w = reinterpret_cast<float*>(base + kOffSum);
                 if (t <= kD) {
-                    float* dst = t < kD ? S_out : z_out;
-                    if (dst) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int fi = 32 * hh + e;
-                            dst[t < kD ? (int64_t)h * kD * kD + fi * kD + t : (int64_t)h * kD + fi] = srun[e];
-                        }
+                    for (int e = 0; e < 32; ++e) sum_w[sum_idx(t, 32 * hh + e)] = srun[e];
+                }
+                named_bar(kBarState, kStateThreads);
+                for (int idx = ts; idx < kE; idx += kStateThreads) {
+                    if (idx < kD * kD) {
+                        if (S_out) S_out[(int64_t)h * kD * kD + idx] = sum_w[idx];
+                    } else if (z_out) {
+                        z_out[(int64_t)h * kD + idx - kD * kD] = sum_w[idx];
                     }
                 }
 #pragma unroll

@@ -109,6 +109,23 @@ __device__ __forceinline__ void phi_tile_256(uint8_t* tile, int t, int zero_from
     }
 }
 
+// phi_tile_256 on two tiles at once: all eight loads are issued before any
+// store, so the two tiles' shared-memory latencies overlap.
+__device__ __forceinline__ void phi_tiles2_256(uint8_t* ta, int zero_a, uint8_t* tb, int zero_b,
+                                               int t) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        v[k] = *reinterpret_cast<const uint4*>((k < 4 ? ta : tb) +
+                                               ((t >> 3) + 32 * (k & 3)) * 128 + (t & 7) * 16);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = (t >> 3) + 32 * (k & 3);
+        const uint4 o = r < (k < 4 ? zero_a : zero_b) ? phi8(v[k]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>((k < 4 ? ta : tb) + r * 128 + (t & 7) * 16) = o;
+    }
+}
+
 // The "ones" operand tile: 128 rows, logical column 0 = 1.0, the rest 0.
 __device__ __forceinline__ void init_ones_tile(uint8_t* tile, int t, int nthreads) {
     for (int idx = t; idx < kC * 8; idx += nthreads) {

@@ -258,9 +258,11 @@ def test_tc_causal_partitions(la, B, H, N):
     assert err <= TOL["bf16"], err
 
 
-def test_tc_causal_final_state(la):
-    B, H, N = 2, 3, 1500
-    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=21)
+@pytest.mark.parametrize("B,H,N", [(2, 3, 1500), (4, 64, 200), (8, 64, 100)])
+def test_tc_causal_final_state(la, B, H, N):
+    # (4, 64, 200) and (8, 64, 100): ranges of three or more chunks hold several
+    # head ends, so one CTA writes several final states.
+    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=21 + N)
     dev = torch.device("cuda")
     S = torch.full((B, H, 64, 64), float("nan"), device=dev)
     z = torch.full((B, H, 64), float("nan"), device=dev)
