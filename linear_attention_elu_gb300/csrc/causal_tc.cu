@@ -56,19 +56,26 @@ using namespace tcc;
 constexpr int kD = 64;                         // Dk = Dv
 constexpr int kE = kD * kD + kD;               // floats per published sum (S row-major, then z)
 
-// Warp roles (22 warps):
-//   warps 0-3   phi:   phi on the K (and Q) tiles of each landed slot or stage, in place
-//   warps 4-11  epi:   two warps per TMEM lane quarter. Once per range: publish
+// Warp roles (24 warps):
+//   warps 0-7   phi:   phi on the K (and Q) tiles of each landed slot or stage, in
+//                      place; its first thread issues MMA (1) of the chunk when the
+//                      chunk's TMEM buffer is already free (see below)
+//   warps 8-15  epi:   two warps per TMEM lane quarter. Once per range: publish
 //                      the last run's sum, look back, seed the running state.
-//                      Per chunk: A (fp32, TMEM) -> causal mask -> bf16 P in the
-//                      same TMEM columns (A operand of MMA (4)); then the output
-//                      num / (den + eps) of the previous chunk
-//   warps 12-14, 16-18 state: running state [S^T ; z] in registers (TMEM lanes
+//                      Then warps 8-11 (mask): A (fp32, TMEM) -> causal mask ->
+//                      bf16 P in the same TMEM columns, and their first thread
+//                      issues MMA (4) and, once the state rows are written, (3);
+//                      warps 12-15 (output): num / (den + eps) to global memory
+//   warps 16-18, 20-22 state: running state [S^T ; z] in registers (TMEM lanes
 //                      0-95, two warps per lane quarter, 32 columns each): adds
 //                      each chunk's [dS ; dz], writes the bf16 state rows of the
 //                      next chunk and the final head states
-//   warp 15     TMA producer
-//   warp 19     MMA (1)       warp 20  MMA (4), (3)       warp 21  MMA (2)
+//   warp 19     TMA producer
+//   warp 23     MMA (2); allocates and frees TMEM
+// MMA (1) of chunk i >= 2 needs phi of chunk i and the output warps' reads of
+// chunk i - 2 (same TMEM buffer): both sides count themselves in on a shared
+// counter and the one that arrives second issues it, so neither waits for a
+// wake-up from the other.
 // Per chunk i of the range (stage s, TMEM buffer b = i mod 2):
 //   (1) A           = phi(Q) phi(K)^T                     M=128, N=128, K=64
 //   (4) [num | den] = P [V | 1]                            M=128, N=80,  K=128
@@ -82,7 +89,7 @@ constexpr int kE = kD * kD + kD;               // floats per published sum (S ro
 // shared memory; step 3 loads start once step 1 has released it.
 constexpr int kPhiWarps = 8;
 constexpr int kEpiW0 = kPhiWarps, kStateW0 = kEpiW0 + 8;       // state: 16-18 and 20-22
-constexpr int kProdW = kStateW0 + 3, kQkW = kProdW + 4, kPvW = kQkW + 1, kStW = kPvW + 1;
+constexpr int kProdW = kStateW0 + 3, kStW = kProdW + 4;
 constexpr int kThreads = 32 * (kStW + 1);
 constexpr int kPhiThreads = 32 * kPhiWarps;
 constexpr int kEpiThreads = 256;
@@ -113,9 +120,10 @@ constexpr uint32_t kTmState = 448;                             // running state:
 struct Misc {
     uint64_t afull[kSlots], aphi[kSlots], aempty[kSlots];
     uint64_t full[kStages], phi_done[kStages], empty[kStages];
-    uint64_t snap_ready[kStages], a_full[2], p_full[2], o_full[2], o_free[2];
-    uint64_t a_done, ds_full[2], ds_free[2], drain[3];
+    uint64_t snap_ready[kStages], a_full[2], o_full[2];
+    uint64_t a_done, ds_full[2], ds_free[2], drain[4];
     uint32_t tmem_slot;
+    int qk_arrive[2];                          // arrivals for MMA (1), per TMEM buffer
     int walk_stop, walk_incl;
 };
 
@@ -229,11 +237,10 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&m.a_full[b], 1);
-            mbar_init(&m.p_full[b], 1);
             mbar_init(&m.o_full[b], 1);
-            mbar_init(&m.o_free[b], 1);
+            m.qk_arrive[b] = 0;
         }
-        for (int d = 0; d < 3; ++d) mbar_init(&m.drain[d], 1);
+        for (int d = 0; d < 4; ++d) mbar_init(&m.drain[d], 1);
         mbar_init(&m.a_done, 1);
         for (int d = 0; d < 2; ++d) {
             mbar_init(&m.ds_full[d], 1);
@@ -243,7 +250,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     if (warp < kProdW) init_ones_tile(ones, tid, 32 * kProdW);
     fence_proxy_async_smem();
-    if (warp == kQkW) {
+    if (warp == kStW) {
         tmem_alloc(&m.tmem_slot, 512);
         tmem_relinquish();
     }
@@ -263,6 +270,29 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const uint32_t onesa = smem_u32(ones);
+    // MMA (1) of range chunk i into TMEM buffer i mod 2, then a_full.
+    auto issue_qk = [&](int i) {
+        const int s = i % kStages, b = i & 1;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(stage(s) + kStQ), ka = smem_u32(stage(s) + kStK);
+        const uint32_t tbuf = tmem + kTmBuf * b;
+        const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+        for (int k16 = 0; k16 < kD / 16; ++k16)
+            mma_bf16(tbuf, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
+                     smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_qk, k16 > 0);
+        mma_commit(&m.a_full[b]);
+    };
+    // One of the two arrivals (phi of chunk i, output reads of chunk i - 2) for
+    // MMA (1) of chunk i >= 2 on TMEM buffer b; true for the second one, whose
+    // thread then issues it. Arrivals alternate, so the counter's old value is
+    // odd exactly for the second.
+    auto qk_second = [&](int b) -> bool {
+        __threadfence_block();
+        const int prev = atomicAdd(&m.qk_arrive[b], 1);
+        __threadfence_block();
+        return (prev & 1) != 0;
+    };
 
     if (warp == kProdW) {
         // ---------------------------------------------------------- producer
@@ -346,68 +376,6 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             mma_commit(&m.drain[2]);  // every issued MMA completes before TMEM is released
             mbar_wait(&m.drain[2], 0, kDefaultMaxSpin);
         }
-    } else if (warp == kQkW) {
-        // ---------------------------------------------------------- MMA (1)
-        if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-            bool ok = true;
-            for (int i = 0; i < nch && ok; ++i) {
-                const int s = i % kStages, b = i & 1;
-                if (!mbar_wait(&m.phi_done[s], (i / kStages) & 1, max_spin) ||
-                    (i >= 2 && !mbar_wait(&m.o_free[b], ((i >> 1) - 1) & 1, max_spin))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t qa = smem_u32(stage(s) + kStQ), ka = smem_u32(stage(s) + kStK);
-                const uint32_t tbuf = tmem + kTmBuf * b;
-#pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tbuf, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_qk, k16 > 0);
-                mma_commit(&m.a_full[b]);
-            }
-            if (!ok) report_timeout(hdr);
-            mma_commit(&m.drain[0]);
-            mbar_wait(&m.drain[0], 0, kDefaultMaxSpin);
-        }
-    } else if (warp == kPvW) {
-        // ---------------------------------------------------------- MMA (4), (3)
-        if (lane == 0) {
-            const uint32_t id_pv = idesc_bf16_f32(128, 80, false, true);
-            const uint32_t id_qs = idesc_bf16_f32(128, 80, false, false);
-            bool ok = true;
-            for (int j = 0; j < nch; ++j) {
-                const int sj = j % kStages, bj = j & 1;
-                if (!mbar_wait(&m.p_full[bj], (j >> 1) & 1, max_spin)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t va = smem_u32(stage(sj) + kStV);
-                const uint32_t lbo = onesa - va;
-                const uint32_t tbuf = tmem + kTmBuf * bj;
-#pragma unroll
-                for (int k16 = 0; k16 < kC / 16; ++k16)
-                    mma_bf16_ts(tbuf + kTmNum, tbuf + 8 * k16,
-                                smem_desc(va + k16 * 2048, lbo, 1024, kSwizzle128B), id_pv, k16 > 0);
-                if (!mbar_wait(&m.snap_ready[sj], (j / kStages) & 1, max_spin)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t qa = smem_u32(stage(sj) + kStQ), sa = smem_u32(stage(sj) + kStS);
-#pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tbuf + kTmNum, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(sa + k16 * 32, 16, 1024, kSwizzle128B), id_qs, 1u);
-                mma_commit(&m.o_full[bj]);
-                mma_commit(&m.empty[sj]);  // (1) of chunk j completed before P existed
-            }
-            if (!ok) report_timeout(hdr);
-            mma_commit(&m.drain[1]);
-            mbar_wait(&m.drain[1], 0, kDefaultMaxSpin);
-        }
     } else if (warp < kEpiW0) {
         // ---------------------------------------------------------- phi role
         const int t = tid;
@@ -420,16 +388,30 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             ok = named_bar_and(kBarPhi, kPhiThreads, ok);
             if (ok && t == 0) mbar_arrive(&m.aphi[a % kSlots]);
         }
-        for (int i = 0; i < nch && ok; ++i) {
+        // The first thread's own wait may fail after the barrier; it then carries
+        // ok = false into the next barrier, which every phi thread still reaches.
+        for (int i = 0; i < nch; ++i) {
             const int s = i % kStages;
             const int ch = (int)((u0 + i) % nchunks);
-            ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
-            phi_tiles2_256(stage(s) + kStK, min(kC, N - ch * kC), stage(s) + kStQ, kC, t);
+            if (ok) ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
+            if (ok) phi_tiles2_256(stage(s) + kStK, min(kC, N - ch * kC), stage(s) + kStQ, kC, t);
             fence_proxy_async_smem();
             ok = named_bar_and(kBarPhi, kPhiThreads, ok);
-            if (ok && t == 0) mbar_arrive(&m.phi_done[s]);
+            if (!ok) break;
+            if (t == 0) {
+                mbar_arrive(&m.phi_done[s]);
+                // Count in for (1) only once (1) of chunk i - 2 was issued, so that the
+                // two arrivals of one chunk are never mixed with the next chunk's on
+                // the same buffer (the output side cannot run ahead: it waits for (3)).
+                if (i >= 4) ok = mbar_wait(&m.a_full[i & 1], ((i - 2) >> 1) & 1, max_spin);
+                if (ok && (i < 2 || qk_second(i & 1))) issue_qk(i);
+            }
         }
-        if (!ok && t == 0) report_timeout(hdr);
+        if (t == 0) {
+            if (!ok) report_timeout(hdr);
+            mma_commit(&m.drain[0]);  // every issued MMA completes before TMEM is released
+            mbar_wait(&m.drain[0], 0, kDefaultMaxSpin);
+        }
     } else if (warp < kEpiW0 + 8) {
         // ---------------------------------------------------------- epi role
         // Thread (quarter q4, half hh, lane) owns TMEM lane v = 32 q4 + lane and,
@@ -576,14 +558,20 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             // A block j (32 keys, columns 32j..32j+31) -> P block j (16 packed
             // columns 16j..16j+15) in the same TMEM buffer; in increasing j every A
             // column is read before the P columns that cover it are written. Blocks
-            // past the diagonal block q4 are zero for this lane quarter.
+            // past the diagonal block q4 are zero for this lane quarter. The first
+            // thread then issues (4) [num | den] = P [V | 1] and, once the state
+            // rows of the chunk are written, (3) += phi(Q) [S^T | z]. Its waits may
+            // fail after the barrier: it then carries ok = false into the next
+            // barrier, which every mask thread still reaches.
             const int tm = t;                             // 0..127
-            for (int i = 0; i < nch && ok; ++i) {
-                const int b = i & 1;
+            const uint32_t id_pv = idesc_bf16_f32(128, 80, false, true);
+            const uint32_t id_qs = idesc_bf16_f32(128, 80, false, false);
+            for (int i = 0; i < nch; ++i) {
+                const int b = i & 1, s = i % kStages;
                 const uint32_t tbuf = tmem + kTmBuf * b + lane_base;
-                ok = mbar_wait(&m.a_full[b], (i >> 1) & 1, max_spin);
+                if (ok) ok = mbar_wait(&m.a_full[b], (i >> 1) & 1, max_spin);
                 tc_fence_after();
-                for (int j = 0; j <= q4; ++j) {
+                for (int j = 0; ok && j <= q4; ++j) {
                     uint32_t r0[16], r1[16];
                     tmem_ld16(tbuf + 32 * j, r0);
                     tmem_ld16(tbuf + 32 * j + 16, r1);
@@ -601,7 +589,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                                              17 + 2 * e <= lim ? __uint_as_float(r1[2 * e + 1]) : 0.f);
                     tmem_st16(tbuf + 16 * j, p);
                 }
-                for (int j = q4 + 1; j < 4; ++j) {
+                for (int j = q4 + 1; ok && j < 4; ++j) {
                     uint32_t p[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) p[e] = 0u;
@@ -611,13 +599,39 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 tc_fence_before();
                 ok = named_bar_and(kBarPair, 128, ok);
                 if (!ok) break;
-                if (tm == 0) mbar_arrive(&m.p_full[b]);
+                if (tm == 0) {
+                    tc_fence_after();
+                    const uint32_t va = smem_u32(stage(s) + kStV);
+                    const uint32_t lbo = onesa - va;
+                    const uint32_t tb = tmem + kTmBuf * b;
+#pragma unroll
+                    for (int k16 = 0; k16 < kC / 16; ++k16)
+                        mma_bf16_ts(tb + kTmNum, tb + 8 * k16,
+                                    smem_desc(va + k16 * 2048, lbo, 1024, kSwizzle128B), id_pv,
+                                    k16 > 0);
+                    ok = mbar_wait(&m.snap_ready[s], (i / kStages) & 1, max_spin);
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(stage(s) + kStQ), sa = smem_u32(stage(s) + kStS);
+#pragma unroll
+                        for (int k16 = 0; k16 < kD / 16; ++k16)
+                            mma_bf16(tb + kTmNum, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
+                                     smem_desc(sa + k16 * 32, 16, 1024, kSwizzle128B), id_qs, 1u);
+                        mma_commit(&m.o_full[b]);
+                        mma_commit(&m.empty[s]);  // (1) of the chunk completed before P existed
+                    }
+                }
             }
-            if (!ok && tm == 0) report_timeout(hdr);
+            if (tm == 0) {
+                if (!ok) report_timeout(hdr);
+                mma_commit(&m.drain[1]);
+                mbar_wait(&m.drain[1], 0, kDefaultMaxSpin);
+            }
         } else {
             // ------------------------------------------------------ output (warps 12-15)
             // Thread = query row v of its lane quarter. The TMEM buffer is released
-            // as soon as num and den are in registers (scaled and packed to bf16).
+            // as soon as num and den are in registers (scaled and packed to bf16):
+            // the first thread counts in for MMA (1) of chunk j + 2.
             const int to_t = t - 128;                     // 0..127
             for (int j = 0; j < nch && ok; ++j) {
                 const int bj = j & 1;
@@ -651,7 +665,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 ok = named_bar_and(kBarPair + 1, 128, ok);
                 if (!ok) break;
                 if (to_t == 0) {
-                    mbar_arrive(&m.o_free[bj]);
+                    if (j + 2 < nch && qk_second(bj)) issue_qk(j + 2);
                     tma_store_wait_read<0>();             // the staging tile is free again
                 }
                 named_bar(kBarPair + 1, 128);
@@ -666,8 +680,12 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     tma_store_commit();
                 }
             }
-            if (!ok && to_t == 0) report_timeout(hdr);
-            if (to_t == 0) tma_store_wait_all<0>();
+            if (to_t == 0) {
+                if (!ok) report_timeout(hdr);
+                tma_store_wait_all<0>();
+                mma_commit(&m.drain[3]);
+                mbar_wait(&m.drain[3], 0, kDefaultMaxSpin);
+            }
         }
     } else {
         // ---------------------------------------------------------- state role
@@ -750,7 +768,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kQkW) {
+    if (warp == kStW) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
