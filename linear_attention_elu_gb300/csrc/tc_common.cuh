@@ -52,16 +52,15 @@ __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u <<
 
 // phi(x) = max(x, 0) + min(2^(x log2 e), 1) on two packed bf16 values: equal
 // to x + 1 for x > 0 and e^x for x <= 0 (e^x >= 1 exactly when x >= 0).
-// x log2 e is formed as x*c_hi + x*c_lo with c_hi + c_lo = log2 e to about
-// 2^-17, rounded once to bf16; the power of two is the hardware ex2.
+// x log2 e is one bf16 fma with bf16(log2 e) = 1.4453125 (0.18 % above log2 e),
+// rounded once to bf16; the power of two is the hardware ex2. Five packed
+// instructions per two values; the result is within 1.7 % of e^x (x <= 0).
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-    constexpr uint32_t kLog2eHi = 0x3FB93FB9u;  // bf16(log2 e) = 1.4453125, twice
-    constexpr uint32_t kLog2eLo = 0xBB2CBB2Cu;  // bf16(log2 e - 1.4453125) = -0.00262451, twice
+    constexpr uint32_t kLog2e = 0x3FB93FB9u;    // bf16(log2 e) = 1.4453125, twice
     constexpr uint32_t kOne = 0x3F803F80u;
     constexpr uint32_t kNegZero = 0x80008000u;
-    uint32_t lo, t, e, m, p, r;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(x), "r"(kLog2eLo), "r"(kNegZero));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eHi), "r"(lo));
+    uint32_t t, e, m, p, r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2e), "r"(kNegZero));
     asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
     asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(e), "r"(kOne));
     asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(x), "r"(0u));
