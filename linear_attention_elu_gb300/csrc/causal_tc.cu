@@ -127,15 +127,6 @@ struct Misc {
     int walk_stop, walk_incl;
 };
 
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Published sums are tagged words: bits of the fp32 value in the low half, the
 // launch tag (epoch + 1) in the high half, stored and loaded as single 64-bit
 // accesses, so a reader that sees the tag also sees the value: no fence or flag.

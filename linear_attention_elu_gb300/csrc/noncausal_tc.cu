@@ -14,8 +14,11 @@
 //                 reduction), laid out once in shared memory as the K-major
 //                 operand [S^T | z_hi | z_lo] (144 rows); per chunk of 128
 //                 queries [num | den] = phi(Q) [S^T | z]^T (M = 128, N = 144,
-//                 K = 128), then o = num / (den + eps). Q is read once, O
-//                 written once.
+//                 K = 128), then o = num / (den + eps). phi(Q) is written to
+//                 TMEM beside the chunk's accumulator as the MMA's A operand,
+//                 so a Q stage is refilled as soon as phi has read it; outputs
+//                 leave through two staging buffers. Q is read once, O written
+//                 once.
 // The apply kernel is a programmatic dependent of the state kernel.
 #include <math.h>
 
@@ -243,7 +246,7 @@ nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 }
 
 // ======================================================== apply kernel
-// Warps 0-7: phi on Q. Warps 8-15: operand build (per run) and output epilogue
+// Warps 0-7: phi on Q into TMEM. Warps 8-15: operand build (per run) and output epilogue
 // (two warps per TMEM lane quarter, each half the value columns).
 // Warp 16: TMA producer. Warp 17: MMA issuer.
 
@@ -251,10 +254,31 @@ constexpr int kAStages = 3;
 constexpr uint32_t kAStage = 2 * kTileBytes;               // Q0 Q1 (32 KB)
 constexpr uint32_t kBSub = kNb * 128;                      // one 64-feature sub-tile of [S^T | z]
 constexpr uint32_t kOffB = kAStages * kAStage;
-constexpr uint32_t kOffO = kOffB + 2 * kBSub;              // output staging (2 boxes)
-constexpr size_t kASmem = 1024 + kOffO + 2 * kTileBytes;
+constexpr uint32_t kOffO = kOffB + 2 * kBSub;              // output staging: 2 buffers of 2 boxes
+constexpr size_t kASmem = 1024 + kOffO + 4 * kTileBytes;
 constexpr int kAThreads = 576;
 constexpr uint32_t kTmStride = 256;                        // TMEM buffer b at 256 b (144 columns)
+
+// phi of row `row` of a 128 x 64 bf16 box (128-byte swizzle) into 32 TMEM
+// columns at taddr: the kind::f16 A-operand layout (two features per column).
+__device__ __forceinline__ void phi_row_to_tmem(const uint8_t* tile, uint32_t taddr, int row) {
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 x = phi8(*reinterpret_cast<const uint4*>(
+                tile + row * 128 + (((4 * hlf + c) ^ (row & 7)) << 4)));
+            w[4 * c] = x.x;
+            w[4 * c + 1] = x.y;
+            w[4 * c + 2] = x.z;
+            w[4 * c + 3] = x.w;
+        }
+        tmem_st16(taddr + 16 * hlf, w);
+    }
+}
+
+constexpr uint32_t kTmQ = 144;                              // phi(Q) of buffer b at +144 (64 columns)
 
 struct ApplyMisc {
     uint64_t full[kAStages], empty[kAStages], phi_done[kAStages];
@@ -348,15 +372,12 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 if (first_in_run) ++run;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(stage(s));
 #pragma unroll
                 for (int k16 = 0; k16 < kD / 16; ++k16)
-                    mma_bf16(tmem + kTmStride * b,
-                             smem_desc(qa + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(ba + (k16 >> 2) * kBSub + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
-                             idesc, k16 > 0);
+                    mma_bf16_ts(tmem + kTmStride * b, tmem + kTmStride * b + kTmQ + 8 * k16,
+                           smem_desc(ba + (k16 >> 2) * kBSub + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
+                           idesc, k16 > 0);
                 mma_commit(&m.o_full[b]);
-                mma_commit(&m.empty[s]);
             }
             if (!ok) report_timeout(hdr);
             mma_commit(&m.mma_drain);
@@ -366,15 +387,26 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         // ---------------------------------------------------------- phi on Q
         const int t = tid;
         bool ok = true;
+        // phi(Q) goes to TMEM next to the chunk's accumulator (the MMA's A
+        // operand), so the stage is free as soon as it has been read.
+        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
         for (int i = 0; i < nch; ++i) {
-            const int s = i % kAStages;
+            const int s = i % kAStages, b = i & 1;
             ok = mbar_wait(&m.full[s], (i / kAStages) & 1, max_spin);
-            phi_tile_256(stage(s), t, kC);
-            phi_tile_256(stage(s) + kTileBytes, t, kC);
-            fence_proxy_async_smem();
+            // The buffer's previous chunk (i - 2) finished its MMA.
+            if (ok && i >= 2) ok = mbar_wait(&m.o_full[b], ((i - 2) >> 1) & 1, max_spin);
+            tc_fence_after();
+            if (ok)
+                phi_row_to_tmem(stage(s) + (warp >> 2) * kTileBytes,
+                                tmem + kTmStride * b + kTmQ + 32 * (warp >> 2) + lb, 32 * (warp & 3) + lane);
+            tmem_st_wait();
+            tc_fence_before();
             ok = named_bar_and(1, 256, ok);
             if (!ok) break;
-            if (t == 0) mbar_arrive(&m.phi_done[s]);
+            if (t == 0) {
+                mbar_arrive(&m.empty[s]);
+                mbar_arrive(&m.phi_done[s]);
+            }
         }
         if (!ok && t == 0) report_timeout(hdr);
     } else {
@@ -435,7 +467,7 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             // output was read below), so the operand can be rebuilt.
             if (i == 0 || ch == 0) build(h);
             ok = mbar_wait(&m.o_full[b], (i >> 1) & 1, max_spin);
-            if (t == 0) tma_store_wait_read<0>();  // the staging tile is free again
+            if (t == 0) tma_store_wait_read<1>();  // staging buffer b (chunk i - 2) is free again
             named_bar(2, 256);
             tc_fence_after();
             const uint32_t to = tmem + kTmStride * b + lane_base;
@@ -446,7 +478,7 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 tmem_ld_wait();
                 inv = 1.f / (__uint_as_float(rd[0]) + __uint_as_float(rd[1]) + eps);
             }
-            uint8_t* ot = ostage + g * kTileBytes;   // value columns [64g, 64g + 64)
+            uint8_t* ot = ostage + (2 * b + g) * kTileBytes;   // value columns [64g, 64g + 64)
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t r0[16], r1[16];
@@ -471,8 +503,8 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (!ok) break;
             if (t == 0) {
                 mbar_arrive(&m.o_free[b]);
-                tma_store_3d(&omap, ostage, 0, ch * kC, h);
-                tma_store_3d(&omap, ostage + kTileBytes, 64, ch * kC, h);
+                tma_store_3d(&omap, ostage + 2 * b * kTileBytes, 0, ch * kC, h);
+                tma_store_3d(&omap, ostage + (2 * b + 1) * kTileBytes, 64, ch * kC, h);
                 tma_store_commit();
             }
         }
