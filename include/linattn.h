@@ -155,6 +155,34 @@ la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, voi
                                 float* S_out, float* z_out, la_stream_t stream);
 
 /*
+ * Causal forward on HOST buffers: q, k, v, o are host pointers in the layout of
+ * la_causal_fwd ([B,H,N,D], dtype dt), S_out / z_out device pointers (nullable),
+ * as in la_causal_fwd. The heads are processed in up to four groups that
+ * stream through two device staging buffers, so that copying a group in,
+ * computing the previous one and copying the one before out overlap (separate
+ * copy engines for the two directions). Each group is an la_causal_fwd call on
+ * its slice of heads (heads are independent; the result equals la_causal_fwd's
+ * up to the order of fp32 additions across CTAs). Host buffers should be
+ * page-locked (cudaHostAlloc / cudaHostRegister): with pageable memory the
+ * copies are still correct but do not overlap.
+ *  - staging: device memory of at least la_host_staging_size() bytes, 256-byte
+ *    aligned, owned by the caller; workspace as for la_causal_fwd at (B, H, N).
+ *  - The call is asynchronous on `stream`: it starts after the work already
+ *    queued there and `stream` waits for the last output copy. On first use on
+ *    a device it creates two streams and eight events for that device (no device
+ *    memory), kept until the process exits; concurrent calls on one device are
+ *    serialised while they enqueue.
+ *  - Returns LA_ERR_WORKSPACE if the staging buffer is missing, misaligned or
+ *    too small, and otherwise what la_causal_fwd returns for a group.
+ */
+la_status la_host_staging_size(int B, int H, int N, int Dk, int Dv, la_dtype dt, size_t* bytes);
+
+la_status la_causal_fwd_host(const void* q, const void* k, const void* v, void* o,
+                             int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                             float* S_out, float* z_out, void* staging, size_t staging_bytes,
+                             void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
  * One recurrent decode step for B*H independent heads, in place:
  * S <- S + phi(k) v^T, z <- z + phi(k), o = phi(q)^T S / (phi(q)^T z + eps).
  * q, k: [B,H,Dk]; v, o: [B,H,Dv] in dtype dt; S: [B,H,Dk,Dv] and z: [B,H,Dk]

@@ -20,7 +20,7 @@ __all__ = [
     "LA_F32", "LA_BF16", "LA_OP_NONCAUSAL", "LA_OP_CAUSAL", "LA_OP_DECODE", "LinAttnError",
     "la_status_string", "la_version", "la_workspace_size", "la_launch_count", "la_workspace_init",
     "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
-    "library_path",
+    "la_host_staging_size", "host_staging", "la_causal_fwd_host", "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
@@ -62,6 +62,10 @@ def _load():
     lib.la_noncausal_fwd.restype = I
     lib.la_causal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P]
     lib.la_causal_fwd.restype = I
+    lib.la_host_staging_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
+    lib.la_host_staging_size.restype = I
+    lib.la_causal_fwd_host.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P, Z, P]
+    lib.la_causal_fwd_host.restype = I
     lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
     lib.la_decode_step.restype = I
     lib.la_query_status.argtypes = [P, P]
@@ -179,6 +183,48 @@ def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, st
                               float(eps), _ptr(S_out), _ptr(z_out), _ptr(ws), ws.numel(),
                               _stream(stream)),
            "la_causal_fwd")
+    return o
+
+
+def la_host_staging_size(B, H, N, Dk, Dv, dtype):
+    """Device staging bytes la_causal_fwd_host needs at this shape."""
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    n = ctypes.c_size_t(0)
+    _check(_lib.la_host_staging_size(B, H, N, Dk, Dv, dt, ctypes.byref(n)), "la_host_staging_size")
+    return int(n.value)
+
+
+def host_staging(B, H, N, Dk, Dv, dtype, device=None):
+    """Allocates (through PyTorch) the device staging buffer of la_causal_fwd_host."""
+    n = la_host_staging_size(B, H, N, Dk, Dv, dtype)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def la_causal_fwd_host(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, staging=None, ws=None,
+                       device=None, stream=None):
+    """Causal forward on host (CPU) tensors, transfers overlapped with compute; returns o on the
+    host. q, k, v should be pinned (tensor.pin_memory()); S_out, z_out are CUDA tensors."""
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous host tensors")
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    if o.is_cuda or not o.is_contiguous() or o.shape != v.shape or o.dtype != v.dtype:
+        raise ValueError("o must be a contiguous host tensor shaped and typed like v")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _need_cuda(S_out, z_out, staging, ws)
+    for t, shp in ((S_out, (B, H, Dk, Dv)), (z_out, (B, H, Dk))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
+            raise ValueError(f"state outputs must be float32 with shape {shp}")
+    if staging is None:
+        staging = host_staging(B, H, N, Dk, Dv, q.dtype, dev)
+    if ws is None:
+        ws = workspace(LA_OP_CAUSAL, B, H, N, Dk, Dv, q.dtype, dev, stream)
+    _check(_lib.la_causal_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                                   float(eps), _ptr(S_out), _ptr(z_out), _ptr(staging),
+                                   staging.numel(), _ptr(ws), ws.numel(), _stream(stream)),
+           "la_causal_fwd_host")
     return o
 
 

@@ -104,3 +104,27 @@ def test_bad_arguments_are_rejected_synchronously(lib):
                             None, 0, None) == 0
     assert so.la_decode_step(None, None, None, None, None, None, 0, 8, 64, 64, 1, 1e-6,
                              None) == 0
+
+
+def test_host_staging_size(lib):
+    # Two buffers of one head group (a quarter of B*H rounded up to a multiple of
+    # 4 heads), each holding q, k, v, o of the group plus 256-byte alignment.
+    per_head = 3072 * (2 * 64 + 2 * 64) * 2
+    assert lib.la_host_staging_size(8, 8, 3072, 64, 64, lib.LA_BF16) == 2 * (16 * per_head + 1024)
+    assert lib.la_host_staging_size(1, 1, 100, 32, 32, lib.LA_F32) == 2 * (4 * 100 * 128 * 4 + 1024)
+    with pytest.raises(lib.LinAttnError):
+        lib.la_host_staging_size(1, 1, 100, 0, 32, lib.LA_F32)
+
+
+def test_host_entry_rejects_bad_arguments_without_a_gpu(lib):
+    raw = _raw(lib)
+    raw.la_causal_fwd_host.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    # Missing host tensors, then a missing staging buffer: rejected before any CUDA call.
+    assert raw.la_causal_fwd_host(None, None, None, None, 1, 1, 8, 64, 64, 1, 1e-6, None, None,
+                                  p, 4096, p, 4096, None) == 1
+    assert raw.la_causal_fwd_host(p, p, p, p, 1, 1, 8, 64, 64, 1, 1e-6, None, None,
+                                  None, 0, p, 4096, None) == 3
