@@ -128,6 +128,27 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
                         void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * Causal forward that continues from a given state: the recurrence starts at
+ * S_0 = S0, z_0 = z0 instead of zero, so that o_i = phi(q_i)^T S_i /
+ * (phi(q_i)^T z_i + eps) with S_i = S0 + sum_{j<=i} phi(k_j) v_j^T and
+ * z_i = z0 + sum_{j<=i} phi(k_j). A long sequence processed in pieces (the
+ * prefill of a prompt in parts, or a prompt extended after decode steps) gives
+ * the result of one call on the whole sequence, up to fp32 rounding, when each
+ * piece starts from the previous piece's S_out, z_out ("Transformers Are RNNs:
+ * Linear Attention", "Turn Causal Attention into a Recurrence": the running
+ * state is all that is carried forward).
+ *  - S0 [B,H,Dk,Dv] and z0 [B,H,Dk]: float32 device pointers, 16-byte aligned,
+ *    both given or both null (null: start from zero, as la_causal_fwd). They
+ *    must not overlap S_out or z_out (LA_ERR_INVALID_ARG): other CTAs may still
+ *    read the initial state while the final state is written.
+ *  - Everything else as la_causal_fwd (same workspace size).
+ */
+la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void* o,
+                              int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                              const float* S0, const float* z0, float* S_out, float* z_out,
+                              void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
  * Causal forward for callers that cannot allocate device memory: a plugin
  * host that passes only input and output buffers, a real-time process that
  * forbids device allocation once it runs, or code whose memory belongs to

@@ -20,7 +20,8 @@ __all__ = [
     "LA_F32", "LA_BF16", "LA_OP_NONCAUSAL", "LA_OP_CAUSAL", "LA_OP_DECODE", "LinAttnError",
     "la_status_string", "la_version", "la_workspace_size", "la_launch_count", "la_workspace_init",
     "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
-    "la_host_staging_size", "host_staging", "la_causal_fwd_host", "library_path",
+    "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
+    "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
@@ -62,6 +63,8 @@ def _load():
     lib.la_noncausal_fwd.restype = I
     lib.la_causal_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P]
     lib.la_causal_fwd.restype = I
+    lib.la_causal_fwd_state.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, Z, P]
+    lib.la_causal_fwd_state.restype = I
     lib.la_host_staging_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
     lib.la_host_staging_size.restype = I
     lib.la_causal_fwd_host.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, Z, P, Z, P]
@@ -183,6 +186,26 @@ def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, st
                               float(eps), _ptr(S_out), _ptr(z_out), _ptr(ws), ws.numel(),
                               _stream(stream)),
            "la_causal_fwd")
+    return o
+
+
+def la_causal_fwd_state(q, k, v, S0, z0, o=None, eps=1e-6, S_out=None, z_out=None, ws=None,
+                        stream=None):
+    """Causal forward continuing from the state (S0 [B,H,Dk,Dv], z0 [B,H,Dk], float32)."""
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, ws, S0, z0, S_out, z_out)
+    for t, shp in ((S0, (B, H, Dk, Dv)), (z0, (B, H, Dk)), (S_out, (B, H, Dk, Dv)),
+                   (z_out, (B, H, Dk))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
+            raise ValueError(f"states must be float32 with shape {shp}")
+    if ws is None:
+        ws = workspace(LA_OP_CAUSAL, B, H, N, Dk, Dv, q.dtype, q.device, stream)
+    _check(_lib.la_causal_fwd_state(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                                    float(eps), _ptr(S0), _ptr(z0), _ptr(S_out), _ptr(z_out),
+                                    _ptr(ws), ws.numel(), _stream(stream)),
+           "la_causal_fwd_state")
     return o
 
 

@@ -64,6 +64,60 @@ __global__ void init_header_kernel(WsHeader* h) { la::init_header(h); }
 
 }  // namespace
 
+namespace {
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+la_status causal_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int N,
+                     int Dk, int Dv, la_dtype dt, float eps, const float* S0, const float* z0,
+                     float* S_out, float* z_out, void* workspace, size_t workspace_bytes,
+                     la_stream_t stream) {
+    la_status s = check_common(B, H, N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if ((s = check_eps(eps)) != LA_OK) return s;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t rows = BH * N;
+    if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
+        (s = check_tensor(v, rows * Dv, dt)) || (s = check_tensor(o, rows * Dv, dt)))
+        return s;
+    if ((S_out && !aligned(S_out, 16)) || (z_out && !aligned(z_out, 16)))
+        return LA_ERR_INVALID_ARG;
+    // The initial state: both parts or neither, aligned, and not overwritten by
+    // the final state while other CTAs may still read it.
+    const size_t s_bytes = sizeof(float) * (size_t)BH * Dk * Dv, z_bytes = sizeof(float) * (size_t)BH * Dk;
+    if ((S0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
+    if (S0 && BH > 0 && (!aligned(S0, 16) || !aligned(z0, 16) ||
+                         overlaps(S0, s_bytes, S_out, s_bytes) || overlaps(S0, s_bytes, z_out, z_bytes) ||
+                         overlaps(z0, z_bytes, S_out, s_bytes) || overlaps(z0, z_bytes, z_out, z_bytes)))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (BH == 0) return LA_OK;
+    if (N == 0) {
+        // Empty sequence: the final state is the initial one (zero when absent).
+        if (S_out && (S0 ? cudaMemcpyAsync(S_out, S0, s_bytes, cudaMemcpyDeviceToDevice, st)
+                         : cudaMemsetAsync(S_out, 0, s_bytes, st)))
+            return LA_ERR_CUDA;
+        if (z_out && (z0 ? cudaMemcpyAsync(z_out, z0, z_bytes, cudaMemcpyDeviceToDevice, st)
+                         : cudaMemsetAsync(z_out, 0, z_bytes, st)))
+            return LA_ERR_CUDA;
+        return LA_OK;
+    }
+    const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL, B, H, N, Dk, Dv, dt);
+    if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
+    char* body = (char*)workspace + kHeaderBytes;
+    if (la::tc_causal_supported(Dk, Dv, dt))
+        return from_cuda(
+            la::tc_causal(q, k, v, o, BH, N, eps, S0, z0, S_out, z_out, workspace, body, st));
+    return from_cuda(
+        la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, S0, z0, S_out, z_out, body, st));
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* la_status_string(la_status s) {
@@ -155,32 +209,16 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, in
                         int N, int Dk, int Dv, la_dtype dt, float eps, float* S_out,
                         float* z_out, void* workspace, size_t workspace_bytes,
                         la_stream_t stream) {
-    la_status s = check_common(B, H, N, Dk, Dv, dt);
-    if (s != LA_OK) return s;
-    if ((s = check_eps(eps)) != LA_OK) return s;
-    const int64_t BH = (int64_t)B * H;
-    const int64_t rows = BH * N;
-    if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
-        (s = check_tensor(v, rows * Dv, dt)) || (s = check_tensor(o, rows * Dv, dt)))
-        return s;
-    if ((S_out && !aligned(S_out, 16)) || (z_out && !aligned(z_out, 16)))
-        return LA_ERR_INVALID_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (BH == 0) return LA_OK;
-    if (N == 0) {
-        // Empty sequence: the final state is the empty sum.
-        if (S_out && cudaMemsetAsync(S_out, 0, sizeof(float) * BH * Dk * Dv, st))
-            return LA_ERR_CUDA;
-        if (z_out && cudaMemsetAsync(z_out, 0, sizeof(float) * BH * Dk, st)) return LA_ERR_CUDA;
-        return LA_OK;
-    }
-    const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL, B, H, N, Dk, Dv, dt);
-    if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
-    char* body = (char*)workspace + kHeaderBytes;
-    if (la::tc_causal_supported(Dk, Dv, dt))
-        return from_cuda(la::tc_causal(q, k, v, o, BH, N, eps, S_out, z_out, workspace, body, st));
-    return from_cuda(
-        la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, S_out, z_out, body, st));
+    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, eps, nullptr, nullptr, S_out, z_out,
+                      workspace, workspace_bytes, stream);
+}
+
+la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void* o, int B,
+                              int H, int N, int Dk, int Dv, la_dtype dt, float eps,
+                              const float* S0, const float* z0, float* S_out, float* z_out,
+                              void* workspace, size_t workspace_bytes, la_stream_t stream) {
+    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, eps, S0, z0, S_out, z_out, workspace,
+                      workspace_bytes, stream);
 }
 
 la_status la_decode_step(const void* q, const void* k, const void* v, void* o, float* S,

@@ -174,12 +174,22 @@ __device__ __forceinline__ void put_z16(uint8_t* tile, int row, int c0, const fl
 // Element (column f, TMEM lane v) of a published sum: S[f][v] for v < 64, z[f] for v = 64.
 __device__ __forceinline__ int sum_idx(int v, int f) { return v < kD ? f * kD + v : kD * kD + f; }
 
+// Element idx (sum_idx layout) of the initial state of head h: S0[h][f][v], z0[h][f].
+__device__ __forceinline__ float init_elem(const float* S0, const float* z0, int64_t h, int idx) {
+    return idx < kD * kD ? S0[h * kD * kD + idx] : z0[h * kD + idx - kD * kD];
+}
+
+// kInit: the recurrence starts from (S0, z0) instead of zero. A separate
+// instantiation: the extra code costs the zero-start kernel several µs (this
+// kernel's timing is sensitive to code added anywhere in it).
+template <bool kInit>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap omap, uint64_t* __restrict__ agg,
-                    uint64_t* __restrict__ incl, float* __restrict__ S_out,
+                    uint64_t* __restrict__ incl, const float* __restrict__ S0,
+                    const float* __restrict__ z0, float* __restrict__ S_out,
                     float* __restrict__ z_out, Partition part, int N, float eps, WsHeader* hdr) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -429,7 +439,10 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int idx = sum_idx(v, 32 * hh + e);
-                    const float x = __uint_as_float(r[e >> 4][e & 15]);
+                    float x = __uint_as_float(r[e >> 4][e & 15]);
+                    // A last run that starts its head carries the head's initial state.
+                    if constexpr (kInit)
+                        if (last_start % nchunks == 0) x += init_elem(S0, z0, last_start / nchunks, idx);
                     st_tagged(my_agg + idx, x, epoch1);
                     sum_s[idx] = x;
                 }
@@ -493,7 +506,13 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             constexpr int kPer = (kE + kEpiThreads - 1) / kEpiThreads;   // 17
             float acc[kPer];
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+            for (int k = 0; k < kPer; ++k) {
+                // A range that starts its head starts from the head's initial state.
+                const int idx = t + kEpiThreads * k;
+                acc[k] = 0.f;
+                if constexpr (kInit)
+                    if (!use_prefix && idx < kE) acc[k] = init_elem(S0, z0, h0, idx);
+            }
             const uint64_t t0 = global_ns();
             for (int r2 = stop; r2 < cta && ok; ++r2) {
                 const uint64_t* src = (r2 == stop && stop_incl ? incl : agg) + (int64_t)r2 * kE;
@@ -734,8 +753,15 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                         z_out[(int64_t)h * kD + idx - kD * kD] = sum_w[idx];
                     }
                 }
+                // The next head (if this range holds its start) begins at its initial state.
 #pragma unroll
                 for (int e = 0; e < 32; ++e) srun[e] = 0.f;
+                if constexpr (kInit) {
+                    if (next && t <= kD) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) srun[e] = init_elem(S0, z0, h + 1, sum_idx(t, 32 * hh + e));
+                    }
+                }
             }
             if (next) {
                 uint8_t* stn = stage((i + 1) % kStages) + kStS;
@@ -793,8 +819,8 @@ size_t tc_causal_workspace(int64_t BH, int N) {
 int tc_causal_launches() { return 1; }
 
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, float* S_out, float* z_out, void* ws_header, void* scratch,
-                      cudaStream_t st) {
+                      float eps, const float* S0, const float* z0, float* S_out, float* z_out,
+                      void* ws_header, void* scratch, cudaStream_t st) {
     Partition p = make_partition(BH, N, grid_cap());
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     uint64_t* agg = reinterpret_cast<uint64_t*>(scratch);
@@ -804,8 +830,10 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    static std::atomic<int> optin[kMaxDevices];
-    if ((err = ensure_smem_optin(causal_fused_kernel, (int)kSmem, optin))) return err;
+    static std::atomic<int> optin[kMaxDevices], optin_init[kMaxDevices];
+    if ((err = S0 ? ensure_smem_optin(causal_fused_kernel<true>, (int)kSmem, optin_init)
+                  : ensure_smem_optin(causal_fused_kernel<false>, (int)kSmem, optin)))
+        return err;
     // Programmatic stream serialization: the next call's CTAs may be scheduled on
     // SMs as this launch's CTAs finish and run their set-up; the kernel waits
     // (griddepcontrol.wait) before its first global-memory access.
@@ -819,7 +847,8 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, causal_fused_kernel, qm, km, vm, om, agg, incl, S_out, z_out,
+    return cudaLaunchKernelEx(&cfg, S0 ? causal_fused_kernel<true> : causal_fused_kernel<false>,
+                              qm, km, vm, om, agg, incl, S0, z0, S_out, z_out,
                               p, N, eps, hdr);
 }
 

@@ -13,9 +13,11 @@ namespace la {
 size_t simt_causal_workspace(int64_t BH, int N, int D, int M);
 size_t simt_noncausal_workspace(int64_t BH, int N, int D, int M);
 int simt_noncausal_splits(int64_t BH, int N);
+// S0, z0: initial state [BH, D, M] and [BH, D] (fp32, both or neither; null = zero).
 cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                        int64_t BH, int N, int D, int M, float eps, float* S_out, float* z_out,
-                        void* scratch, cudaStream_t st);
+                        int64_t BH, int N, int D, int M, float eps, const float* S0,
+                        const float* z0, float* S_out, float* z_out, void* scratch,
+                        cudaStream_t st);
 cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
                            int64_t BH, int N, int D, int M, float eps, void* scratch,
                            cudaStream_t st);
@@ -25,8 +27,8 @@ bool tc_causal_supported(int D, int M, la_dtype dt);
 size_t tc_causal_workspace(int64_t BH, int N);
 int tc_causal_launches();
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, float* S_out, float* z_out, void* ws_header, void* scratch,
-                      cudaStream_t st);
+                      float eps, const float* S0, const float* z0, float* S_out, float* z_out,
+                      void* ws_header, void* scratch, cudaStream_t st);
 
 // Tensor-core (tcgen05) non-causal path: bf16, Dk = Dv = 128.
 bool tc_noncausal_supported(int D, int M, la_dtype dt);

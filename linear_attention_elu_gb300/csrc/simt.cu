@@ -74,9 +74,11 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const T* __restri
     }
 }
 
-// Exclusive prefix over chunks, in place; the total goes to S_out / z_out.
+// Exclusive prefix over chunks, in place, starting from the initial state
+// (S0, z0; zero when null); the total goes to S_out / z_out.
 // One thread per (bh, element).
-__global__ void chunk_scan_kernel(float* __restrict__ states, float* __restrict__ S_out,
+__global__ void chunk_scan_kernel(float* __restrict__ states, const float* __restrict__ S0,
+                                  const float* __restrict__ z0, float* __restrict__ S_out,
                                   float* __restrict__ z_out, int64_t BH, int nchunks, int D,
                                   int M) {
     const int E = D * M + D;
@@ -85,7 +87,7 @@ __global__ void chunk_scan_kernel(float* __restrict__ states, float* __restrict_
     int64_t bh = gid / E;
     int e = (int)(gid - bh * E);
     float* p = states + bh * nchunks * (int64_t)E + e;
-    float run = 0.f;
+    float run = !S0 ? 0.f : e < D * M ? S0[bh * D * M + e] : z0[bh * D + (e - D * M)];
     for (int c = 0; c < nchunks; ++c) {
         float t = p[(int64_t)c * E];
         p[(int64_t)c * E] = run;
@@ -257,8 +259,8 @@ __global__ void __launch_bounds__(kThreads) nc_apply_kernel(const T* __restrict_
 
 template <typename T>
 cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* o, int64_t BH,
-                             int N, int D, int M, float eps, float* S_out, float* z_out,
-                             float* states, cudaStream_t st) {
+                             int N, int D, int M, float eps, const float* S0, const float* z0,
+                             float* S_out, float* z_out, float* states, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     dim3 grid(nchunks, (unsigned)BH);
     size_t sm1 = sizeof(float) * (size_t)kChunk * (D + M);
@@ -273,8 +275,8 @@ cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* 
         return err;
     chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
     const int64_t total = BH * (int64_t)(D * M + D);
-    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, S_out, z_out, BH,
-                                                                        nchunks, D, M);
+    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, S0, z0, S_out,
+                                                                        z_out, BH, nchunks, D, M);
     chunk_output_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v,
                                                         states, (T*)o, N, D, M, eps);
     return cudaPeekAtLastError();
@@ -328,13 +330,15 @@ size_t simt_noncausal_workspace(int64_t BH, int N, int D, int M) {
 }
 
 cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                        int64_t BH, int N, int D, int M, float eps, float* S_out, float* z_out,
-                        void* scratch, cudaStream_t st) {
+                        int64_t BH, int N, int D, int M, float eps, const float* S0,
+                        const float* z0, float* S_out, float* z_out, void* scratch,
+                        cudaStream_t st) {
     float* states = (float*)scratch;
     if (dt == LA_F32)
-        return simt_causal_impl<float>(q, k, v, o, BH, N, D, M, eps, S_out, z_out, states, st);
-    return simt_causal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, S_out, z_out, states,
-                                           st);
+        return simt_causal_impl<float>(q, k, v, o, BH, N, D, M, eps, S0, z0, S_out, z_out,
+                                       states, st);
+    return simt_causal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, S0, z0, S_out, z_out,
+                                           states, st);
 }
 
 cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
