@@ -66,7 +66,7 @@ typedef enum {
     LA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (see status)   */
 } la_status;
 
-typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2 } la_op;
+typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2, LA_OP_CAUSAL_BWD = 3 } la_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status s);
@@ -126,6 +126,25 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
                         int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
                         float* S_out, float* z_out,
                         void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * Causal backward: given dout = dL/do for the causal forward o of (q, k, v),
+ * writes dq = dL/dq, dk = dL/dk, dv = dL/dv (same layouts and dtype as q, k, v).
+ * With dnum_i = dout_i / den_i and dden_i = -(dout_i . o_i) / den_i, the
+ * gradients are dphi(q_i) = S_i dnum_i + z_i dden_i (a forward prefix sum) and
+ * dphi(k_j) = R_j v_j + r_j, dv_j = R_j^T phi(k_j) with R_j = sum_{i>=j}
+ * phi(q_i) dnum_i^T, r_j = sum_{i>=j} phi(q_i) dden_i (a reverse one), so no
+ * S_i is stored ("Transformers Are RNNs: Linear Attention", "Turn Causal
+ * Attention into a Recurrence", on cumulative-sum gradients); then
+ * dq = dphi(q) phi'(q) with phi'(x) = 1 for x > 0, e^x for x <= 0.
+ *  - fp32 arithmetic for both dtypes; Dk, Dv <= 64 (larger: LA_ERR_UNSUPPORTED).
+ *  - workspace: la_workspace_size(LA_OP_CAUSAL_BWD, ...) bytes, initialised once
+ *    with la_workspace_init.
+ */
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                        void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                        la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                        la_stream_t stream);
 
 /*
  * Causal forward that continues from a given state: the recurrence starts at

@@ -47,6 +47,8 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
         case LA_OP_NONCAUSAL:
             if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N);
             return la::simt_noncausal_workspace(BH, N, Dk, Dv);
+        case LA_OP_CAUSAL_BWD:
+            return la::simt_causal_bwd_workspace(BH, N, Dk, Dv);
         default:
             return 0;
     }
@@ -137,7 +139,8 @@ uint32_t la_version(void) { return (0u << 16) | 1u; }
 la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
                             size_t* bytes) {
     if (!bytes) return LA_ERR_INVALID_ARG;
-    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE)
+    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
+        op != LA_OP_CAUSAL_BWD)
         return LA_ERR_INVALID_ARG;
     la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
@@ -145,6 +148,8 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
         *bytes = 0;
         return LA_OK;
     }
+    if (op == LA_OP_CAUSAL_BWD && (Dk > la::kBwdMaxDim || Dv > la::kBwdMaxDim))
+        return LA_ERR_UNSUPPORTED;
     *bytes = kHeaderBytes + round_up(body_bytes(op, B, H, N, Dk, Dv, dt), 256);
     return LA_OK;
 }
@@ -152,7 +157,8 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
 la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt,
                           int* launches) {
     if (!launches) return LA_ERR_INVALID_ARG;
-    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE)
+    if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
+        op != LA_OP_CAUSAL_BWD)
         return LA_ERR_INVALID_ARG;
     la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
@@ -163,6 +169,8 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
     }
     if (op == LA_OP_DECODE)
         *launches = 1;
+    else if (op == LA_OP_CAUSAL_BWD)
+        *launches = 5;
     else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
         *launches = la::tc_causal_launches();
     else if (op == LA_OP_NONCAUSAL && la::tc_noncausal_supported(Dk, Dv, dt))
@@ -219,6 +227,29 @@ la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void*
                               void* workspace, size_t workspace_bytes, la_stream_t stream) {
     return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, eps, S0, z0, S_out, z_out, workspace,
                       workspace_bytes, stream);
+}
+
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                        void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                        la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                        la_stream_t stream) {
+    la_status s = check_common(B, H, N, Dk, Dv, dt);
+    if (s != LA_OK) return s;
+    if ((s = check_eps(eps)) != LA_OK) return s;
+    if (Dk > la::kBwdMaxDim || Dv > la::kBwdMaxDim) return LA_ERR_UNSUPPORTED;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t rows = BH * N;
+    if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
+        (s = check_tensor(v, rows * Dv, dt)) || (s = check_tensor(dout, rows * Dv, dt)) ||
+        (s = check_tensor(dq, rows * Dk, dt)) || (s = check_tensor(dk, rows * Dk, dt)) ||
+        (s = check_tensor(dv, rows * Dv, dt)))
+        return s;
+    if (rows == 0) return LA_OK;
+    const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL_BWD, B, H, N, Dk, Dv, dt);
+    if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
+    char* body = (char*)workspace + kHeaderBytes;
+    return from_cuda(la::simt_causal_bwd(q, k, v, dout, dq, dk, dv, dt, BH, N, Dk, Dv, eps, body,
+                                         (cudaStream_t)stream));
 }
 
 la_status la_decode_step(const void* q, const void* k, const void* v, void* o, float* S,

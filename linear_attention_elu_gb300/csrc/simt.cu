@@ -308,6 +308,242 @@ cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, voi
     return cudaPeekAtLastError();
 }
 
+// ------------------------------------------------------------ causal backward
+//
+// Gradients of L through o for o_i = num_i / den_i, num_i = phi(q_i)^T S_i,
+// den_i = phi(q_i)^T z_i + eps (S_i, z_i the inclusive prefix sums). With
+// g_i = dL/do_i, dnum_i = g_i / den_i and dden_i = -(g_i . o_i) / den_i:
+//   dphi(q_i) = S_i dnum_i + z_i dden_i
+//   dphi(k_j) = R_j v_j + r_j,   dv_j = R_j^T phi(k_j),
+// with the reverse (suffix) sums R_j = sum_{i>=j} phi(q_i) dnum_i^T and
+// r_j = sum_{i>=j} phi(q_i) dden_i: a forward and a reverse cumulative sum, so
+// no S_i is stored ("Transformers Are RNNs: Linear Attention", "Turn Causal
+// Attention into a Recurrence"). Per chunk of 64 tokens both sums split into
+// the chunk's carried-in state and a masked in-chunk part, as in the forward.
+// dq = dphi(q) * phi'(q) with phi'(x) = 1 (x > 0), e^x (x <= 0) = min(phi(x), 1).
+
+// grid (nchunks, BH): per row dnum (M) and dden into rowg [BH, N, M + 1]; per
+// chunk [dR ; dr] = sum_i phi(q_i) [dnum_i ; dden_i]^T into rstates.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_rows_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const T* __restrict__ dout, const float* __restrict__ states, float* __restrict__ rowg,
+    float* __restrict__ rstates, int N, int D, int M, float eps) {
+    extern __shared__ float sm[];
+    const int ldk = D + 1;
+    float* fQ = sm;                       // [64][D+1]
+    float* fK = fQ + kChunk * ldk;        // [64][D+1]
+    float* sV = fK + kChunk * ldk;        // [64][M]
+    float* sG = sV + kChunk * M;          // [64][M]   g, then dnum
+    float* P = sG + kChunk * M;           // [D][M] then zP [D]
+    float* A = P + D * M + D;             // [64][65]
+    float* den = A + kChunk * (kChunk + 1);   // [64]
+    float* dd = den + kChunk;                 // [64] dden
+    const int c = blockIdx.x, nchunks = gridDim.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * kChunk;
+    const int valid = min(kChunk, N - t0);
+    const int E = D * M + D;
+    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
+    load_rows(sG, M, dout + (bh * N + t0) * M, kChunk, valid, M);
+    const float* st = states + (bh * nchunks + c) * (int64_t)E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) P[e] = st[e];
+    __syncthreads();
+    const float* zP = P + D * M;
+    for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += blockDim.x) {
+        int i = idx >> 6, j = idx & 63;
+        float s = 0.f;
+        if (j <= i && i < valid)
+            for (int cc = 0; cc < D; ++cc) s = fmaf(fQ[i * ldk + cc], fK[j * ldk + cc], s);
+        A[i * (kChunk + 1) + j] = s;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float s = A[i * (kChunk + 1) + lane] + A[i * (kChunk + 1) + lane + 32];
+        for (int cc = lane; cc < D; cc += 32) s = fmaf(fQ[i * ldk + cc], zP[cc], s);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) den[i] = s + eps;
+    }
+    __syncthreads();
+    // o_i (recomputed) -> dnum_i = g_i / den_i and the row dot g_i . o_i, one warp per row.
+    float* rg = rowg + (bh * N + t0) * (int64_t)(M + 1);
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float dot = 0.f;
+        for (int m = lane; m < M; m += 32) {
+            float s = 0.f;
+            for (int j = 0; j <= i; ++j) s = fmaf(A[i * (kChunk + 1) + j], sV[j * M + m], s);
+            for (int cc = 0; cc < D; ++cc) s = fmaf(fQ[i * ldk + cc], P[cc * M + m], s);
+            const float o = s / den[i];
+            const float g = sG[i * M + m];
+            dot = fmaf(g, o, dot);
+            sG[i * M + m] = g / den[i];                   // dnum (a row is owned by one warp)
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        const float ddn = -dot / den[i];
+        if (lane == 0) dd[i] = i < valid ? ddn : 0.f;
+        if (i < valid) {
+            for (int m = lane; m < M; m += 32) rg[(int64_t)i * (M + 1) + m] = sG[i * M + m];
+            if (lane == 0) rg[(int64_t)i * (M + 1) + M] = ddn;
+        }
+    }
+    __syncthreads();
+    float* out = rstates + (bh * nchunks + c) * (int64_t)E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float s = 0.f;
+        if (e < D * M) {
+            int cc = e / M, m = e - cc * M;
+            for (int i = 0; i < valid; ++i) s = fmaf(fQ[i * ldk + cc], sG[i * M + m], s);
+        } else {
+            int cc = e - D * M;
+            for (int i = 0; i < valid; ++i) s = fmaf(fQ[i * ldk + cc], dd[i], s);
+        }
+        out[e] = s;
+    }
+}
+
+// Reverse exclusive sum over chunks, in place: chunk c gets the sum of chunks > c.
+__global__ void chunk_rscan_kernel(float* __restrict__ rstates, int64_t BH, int nchunks, int E) {
+    int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= BH * E) return;
+    int64_t bh = gid / E;
+    int e = (int)(gid - bh * E);
+    float* p = rstates + bh * nchunks * (int64_t)E + e;
+    float run = 0.f;
+    for (int c = nchunks - 1; c >= 0; --c) {
+        float t = p[(int64_t)c * E];
+        p[(int64_t)c * E] = run;
+        run += t;
+    }
+}
+
+// grid (nchunks, BH): dq, dk, dv of the chunk from its carried-in forward state
+// (S_prev, z_prev), the carried-in reverse sums (R_next, r_next) and the rows'
+// dnum, dden.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const float* __restrict__ states, const float* __restrict__ rstates,
+    const float* __restrict__ rowg, T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv,
+    int N, int D, int M) {
+    extern __shared__ float sm[];
+    const int ldk = D + 1;
+    float* fQ = sm;                       // [64][D+1]
+    float* fK = fQ + kChunk * ldk;        // [64][D+1]
+    float* sV = fK + kChunk * ldk;        // [64][M]
+    float* DN = sV + kChunk * M;          // [64][M] dnum
+    float* dd = DN + kChunk * M;          // [64] dden
+    float* P = dd + kChunk;               // [D][M] S_prev, then z_prev [D]
+    float* R = P + D * M + D;             // [D][M] R_next, then r_next [D]
+    float* W = R + D * M + D;             // [64][65] phi(q_i).phi(k_j), j <= i
+    float* G = W + kChunk * (kChunk + 1); // [64][65] v_j.dnum_i + dden_i, j <= i
+    const int c = blockIdx.x, nchunks = gridDim.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * kChunk;
+    const int valid = min(kChunk, N - t0);
+    const int E = D * M + D;
+    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
+    const float* rg = rowg + (bh * N + t0) * (int64_t)(M + 1);
+    for (int idx = threadIdx.x; idx < kChunk * (M + 1); idx += blockDim.x) {
+        int i = idx / (M + 1), m = idx - i * (M + 1);
+        float x = i < valid ? rg[idx] : 0.f;
+        if (m < M) DN[i * M + m] = x;
+        else dd[i] = x;
+    }
+    const float* st = states + (bh * nchunks + c) * (int64_t)E;
+    const float* rs = rstates + (bh * nchunks + c) * (int64_t)E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        P[e] = st[e];
+        R[e] = rs[e];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += blockDim.x) {
+        int i = idx >> 6, j = idx & 63;
+        float w = 0.f, g = 0.f;
+        if (j <= i && i < valid) {
+            for (int cc = 0; cc < D; ++cc) w = fmaf(fQ[i * ldk + cc], fK[j * ldk + cc], w);
+            for (int m = 0; m < M; ++m) g = fmaf(sV[j * M + m], DN[i * M + m], g);
+            g += dd[i];
+        }
+        W[i * (kChunk + 1) + j] = w;
+        G[i * (kChunk + 1) + j] = g;
+    }
+    __syncthreads();
+    // dq: dphi(q_i) = S_prev dnum_i + z_prev dden_i + sum_{j<=i} G_ij phi(k_j).
+    T* dqc = dq + (bh * N + t0) * D;
+    for (int idx = threadIdx.x; idx < kChunk * D; idx += blockDim.x) {
+        int i = idx / D, d = idx - i * D;
+        if (i >= valid) continue;
+        float s = P[D * M + d] * dd[i];
+        for (int m = 0; m < M; ++m) s = fmaf(P[d * M + m], DN[i * M + m], s);
+        for (int j = 0; j <= i; ++j) s = fmaf(G[i * (kChunk + 1) + j], fK[j * ldk + d], s);
+        const float f = fQ[i * ldk + d];
+        dqc[(int64_t)i * D + d] = from_f<T>(s * fminf(f, 1.f));
+    }
+    // dk: dphi(k_j) = R_next v_j + r_next + sum_{i>=j} G_ij phi(q_i).
+    T* dkc = dk + (bh * N + t0) * D;
+    for (int idx = threadIdx.x; idx < kChunk * D; idx += blockDim.x) {
+        int j = idx / D, d = idx - j * D;
+        if (j >= valid) continue;
+        float s = R[D * M + d];
+        for (int m = 0; m < M; ++m) s = fmaf(R[d * M + m], sV[j * M + m], s);
+        for (int i = j; i < valid; ++i) s = fmaf(G[i * (kChunk + 1) + j], fQ[i * ldk + d], s);
+        const float f = fK[j * ldk + d];
+        dkc[(int64_t)j * D + d] = from_f<T>(s * fminf(f, 1.f));
+    }
+    // dv: dv_j = R_next^T phi(k_j) + sum_{i>=j} W_ij dnum_i.
+    T* dvc = dv + (bh * N + t0) * M;
+    for (int idx = threadIdx.x; idx < kChunk * M; idx += blockDim.x) {
+        int j = idx / M, m = idx - j * M;
+        if (j >= valid) continue;
+        float s = 0.f;
+        for (int d = 0; d < D; ++d) s = fmaf(R[d * M + m], fK[j * ldk + d], s);
+        for (int i = j; i < valid; ++i) s = fmaf(W[i * (kChunk + 1) + j], DN[i * M + m], s);
+        dvc[(int64_t)j * M + m] = from_f<T>(s);
+    }
+}
+
+template <typename T>
+cudaError_t simt_causal_bwd_impl(const void* q, const void* k, const void* v, const void* dout,
+                                 void* dq, void* dk, void* dv, int64_t BH, int N, int D, int M,
+                                 float eps, float* states, float* rstates, float* rowg,
+                                 cudaStream_t st) {
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    dim3 grid(nchunks, (unsigned)BH);
+    const size_t sm1 = sizeof(float) * (size_t)kChunk * (D + M);
+    const size_t sm2 = sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + 2 * M) + (size_t)D * M + D +
+                                        kChunk * (kChunk + 1) + 2 * kChunk);
+    const size_t sm3 = sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + 2 * M) + kChunk +
+                                        2 * ((size_t)D * M + D) + 2 * kChunk * (kChunk + 1));
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chunk_state_kernel<T>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
+        (err = cudaFuncSetAttribute(bwd_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sm2)) ||
+        (err = cudaFuncSetAttribute(bwd_grad_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sm3)))
+        return err;
+    const int E = D * M + D;
+    const int64_t total = BH * (int64_t)E;
+    chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
+    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, nullptr, nullptr,
+                                                                        nullptr, nullptr, BH,
+                                                                        nchunks, D, M);
+    bwd_rows_kernel<T><<<grid, kThreads, sm2, st>>>((const T*)q, (const T*)k, (const T*)v,
+                                                    (const T*)dout, states, rowg, rstates, N, D,
+                                                    M, eps);
+    chunk_rscan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(rstates, BH, nchunks, E);
+    bwd_grad_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v, states,
+                                                    rstates, rowg, (T*)dq, (T*)dk, (T*)dv, N, D, M);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace
 
 size_t simt_causal_workspace(int64_t BH, int N, int D, int M) {
@@ -352,6 +588,26 @@ cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o,
                                           st);
     return simt_noncausal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, nsplit, partials,
                                               total, st);
+}
+
+size_t simt_causal_bwd_workspace(int64_t BH, int N, int D, int M) {
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    return sizeof(float) * ((size_t)2 * BH * nchunks * (size_t)(D * M + D) +
+                            (size_t)BH * N * (size_t)(M + 1));
+}
+
+cudaError_t simt_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                            void* dq, void* dk, void* dv, la_dtype dt, int64_t BH, int N, int D,
+                            int M, float eps, void* scratch, cudaStream_t st) {
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    float* states = (float*)scratch;
+    float* rstates = states + (size_t)BH * nchunks * (size_t)(D * M + D);
+    float* rowg = rstates + (size_t)BH * nchunks * (size_t)(D * M + D);
+    if (dt == LA_F32)
+        return simt_causal_bwd_impl<float>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, states,
+                                           rstates, rowg, st);
+    return simt_causal_bwd_impl<__nv_bfloat16>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, states,
+                                               rstates, rowg, st);
 }
 
 }  // namespace la
