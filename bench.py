@@ -237,11 +237,16 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-# Multiply-adds the fp32 causal backward executes per token at Dk = Dv = 64 with
-# 64-token chunks (32.5 in-chunk keys on average): the forward chunk states
-# (4,160), rows pass (12,513: A, den, num, the chunk's reverse sum) and
-# gradient pass (22,848: W, G, dq, dk, dv).
-BWD_MACS_PER_TOKEN_D64 = 4160 + 12513 + 22848
+# Multiply-adds the fp32 backward executes per token at Dk = Dv = 64 with
+# 64-token chunks (32.5 in-chunk keys on average, 32.5 x 64 = 2,080 for a masked
+# in-chunk product). Causal: the chunk states phi(k) [v | 1] (4,160); the rows
+# pass (12,513: A 2,080, den 64 + 32.5, num 2,080 + 4,096, the chunk's reverse
+# sum 4,160); the gradient pass (24,832: W 2,080, G 2,080, dq 4,096 + 2,080 + 64,
+# dk 4,096 + 2,080, dv 4,096 + 2,080). Non-causal, no in-chunk terms: states
+# 4,160; rows 8,320 (den 64, num 4,096, reverse sum 4,160); gradients 12,352
+# (dq 4,096 + 64, dk 4,096, dv 4,096).
+BWD_MACS_PER_TOKEN_D64 = 4160 + 12513 + 24832
+NC_BWD_MACS_PER_TOKEN_D64 = 4160 + 8320 + 12352
 # fp32 FMA peak from the unit counts and clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz.
 FP32_FMA_PEAK = 152 * 128 * 2 * 2.07e9
 
@@ -312,32 +317,38 @@ def other_paths(la, dev, stream):
                      "frac_of_hbm": per_step / (us * 1e-6) / 1e9 / hbm,
                      "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
     del q, k, v, o, S, z, g
-    # Causal backward (fp32 SIMT arithmetic), the image workload B=8 H=8 N=3072 D=64 bf16.
+    # Causal and non-causal backward (fp32 SIMT arithmetic) at the image shape
+    # B=8 H=8 N=3072 D=64 bf16.
     w = WORKLOADS["image"]
     q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
                      for _ in range(4))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = la.workspace(la.LA_OP_CAUSAL_BWD, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
-    la.la_causal_bwd(q, k, v, dout, dq, dk, dv, ws=ws)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        la.la_causal_bwd(q, k, v, dout, dq, dk, dv, ws=ws)
-    g.replay()
-    torch.cuda.synchronize()
-    reps = 5
-    a.record(stream)
-    for _ in range(reps):
+    for key, fn, op, macs, name in (
+            ("causal_bwd", la.la_causal_bwd, la.LA_OP_CAUSAL_BWD, BWD_MACS_PER_TOKEN_D64,
+             w.name.replace("causal", "causal backward")),
+            ("noncausal_bwd", la.la_noncausal_bwd, la.LA_OP_NONCAUSAL_BWD,
+             NC_BWD_MACS_PER_TOKEN_D64, w.name.replace("causal", "non-causal backward"))):
+        ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
+        fn(q, k, v, dout, dq, dk, dv, ws=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(q, k, v, dout, dq, dk, dv, ws=ws)
         g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
-    flops = w.tokens * 2 * BWD_MACS_PER_TOKEN_D64
-    out["causal_bwd"] = {"workload": w.name.replace("causal", "causal backward"),
-                         "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
-                         "tflops": flops / (ms * 1e-3) / 1e12,
-                         "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
-                         "bound": "alu (fp32 FMA)"}
+        torch.cuda.synchronize()
+        reps = 5
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        flops = w.tokens * 2 * macs
+        out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+                    "ms_per_call": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
+                    "bound": "alu (fp32 FMA)"}
+        del ws, g
     return out
 
 

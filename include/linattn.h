@@ -66,7 +66,13 @@ typedef enum {
     LA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (see status)   */
 } la_status;
 
-typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2, LA_OP_CAUSAL_BWD = 3 } la_op;
+typedef enum {
+    LA_OP_NONCAUSAL = 0,
+    LA_OP_CAUSAL = 1,
+    LA_OP_DECODE = 2,
+    LA_OP_CAUSAL_BWD = 3,
+    LA_OP_NONCAUSAL_BWD = 4
+} la_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status s);
@@ -145,6 +151,22 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
                         void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
                         la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
                         la_stream_t stream);
+
+/*
+ * Non-causal backward: the same gradients for the non-causal forward
+ * o_i = phi(q_i)^T S / (phi(q_i)^T z + eps), where S, z and the reverse sums
+ * R = sum_i phi(q_i) dnum_i^T, r = sum_i phi(q_i) dden_i run over the whole
+ * sequence: dphi(q_i) = S dnum_i + z dden_i, dphi(k_j) = R v_j + r,
+ * dv_j = R^T phi(k_j) ("Transformers Are RNNs: Linear Attention", the
+ * associativity rewrite that shares S and z among all queries).
+ *  - fp32 arithmetic for both dtypes; Dk, Dv <= 64 (larger: LA_ERR_UNSUPPORTED).
+ *  - workspace: la_workspace_size(LA_OP_NONCAUSAL_BWD, ...) bytes, initialised
+ *    once with la_workspace_init.
+ */
+la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                           void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                           la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                           la_stream_t stream);
 
 /*
  * Causal forward that continues from a given state: the recurrence starts at

@@ -21,12 +21,12 @@ __all__ = [
     "la_status_string", "la_version", "la_workspace_size", "la_launch_count", "la_workspace_init",
     "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
     "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
-    "la_causal_bwd", "LA_OP_CAUSAL_BWD",
+    "la_causal_bwd", "LA_OP_CAUSAL_BWD", "la_noncausal_bwd", "LA_OP_NONCAUSAL_BWD",
     "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
-LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_CAUSAL_BWD = 0, 1, 2, 3
+LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_BWD = 0, 1, 2, 3, 4
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 
 _DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
@@ -66,6 +66,8 @@ def _load():
     lib.la_causal_fwd.restype = I
     lib.la_causal_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, Z, P]
     lib.la_causal_bwd.restype = I
+    lib.la_noncausal_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, Z, P]
+    lib.la_noncausal_bwd.restype = I
     lib.la_causal_fwd_state.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P, Z, P]
     lib.la_causal_fwd_state.restype = I
     lib.la_host_staging_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
@@ -212,8 +214,7 @@ def la_causal_fwd_state(q, k, v, S0, z0, o=None, eps=1e-6, S_out=None, z_out=Non
     return o
 
 
-def la_causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None):
-    """Gradients (dq, dk, dv) of sum(o * dout) for the causal forward o of (q, k, v)."""
+def _bwd(fn, op, q, k, v, dout, dq, dk, dv, eps, ws, stream):
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if dout.shape != v.shape or dout.dtype != v.dtype:
         raise ValueError("dout must be shaped and typed like v")
@@ -222,12 +223,23 @@ def la_causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, s
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(q, k, v, dout, dq, dk, dv, ws)
     if ws is None:
-        ws = workspace(LA_OP_CAUSAL_BWD, B, H, N, Dk, Dv, q.dtype, q.device, stream)
-    _check(_lib.la_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                              B, H, N, Dk, Dv, _dt(q), float(eps), _ptr(ws), ws.numel(),
-                              _stream(stream)),
-           "la_causal_bwd")
+        ws = workspace(op, B, H, N, Dk, Dv, q.dtype, q.device, stream)
+    _check(getattr(_lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                             B, H, N, Dk, Dv, _dt(q), float(eps), _ptr(ws), ws.numel(),
+                             _stream(stream)),
+           fn)
     return dq, dk, dv
+
+
+def la_causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(o * dout) for the causal forward o of (q, k, v)."""
+    return _bwd("la_causal_bwd", LA_OP_CAUSAL_BWD, q, k, v, dout, dq, dk, dv, eps, ws, stream)
+
+
+def la_noncausal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(o * dout) for the non-causal forward o of (q, k, v)."""
+    return _bwd("la_noncausal_bwd", LA_OP_NONCAUSAL_BWD, q, k, v, dout, dq, dk, dv, eps, ws,
+                stream)
 
 
 def la_host_staging_size(B, H, N, Dk, Dv, dtype):

@@ -48,7 +48,8 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
             if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N);
             return la::simt_noncausal_workspace(BH, N, Dk, Dv);
         case LA_OP_CAUSAL_BWD:
-            return la::simt_causal_bwd_workspace(BH, N, Dk, Dv);
+        case LA_OP_NONCAUSAL_BWD:
+            return la::simt_bwd_workspace(BH, N, Dk, Dv);
         default:
             return 0;
     }
@@ -140,7 +141,7 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
                             size_t* bytes) {
     if (!bytes) return LA_ERR_INVALID_ARG;
     if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
-        op != LA_OP_CAUSAL_BWD)
+        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD)
         return LA_ERR_INVALID_ARG;
     la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
@@ -148,7 +149,8 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
         *bytes = 0;
         return LA_OK;
     }
-    if (op == LA_OP_CAUSAL_BWD && (Dk > la::kBwdMaxDim || Dv > la::kBwdMaxDim))
+    if ((op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD) &&
+        (Dk > la::kBwdMaxDim || Dv > la::kBwdMaxDim))
         return LA_ERR_UNSUPPORTED;
     *bytes = kHeaderBytes + round_up(body_bytes(op, B, H, N, Dk, Dv, dt), 256);
     return LA_OK;
@@ -158,7 +160,7 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
                           int* launches) {
     if (!launches) return LA_ERR_INVALID_ARG;
     if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
-        op != LA_OP_CAUSAL_BWD)
+        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD)
         return LA_ERR_INVALID_ARG;
     la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
@@ -169,7 +171,7 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
     }
     if (op == LA_OP_DECODE)
         *launches = 1;
-    else if (op == LA_OP_CAUSAL_BWD)
+    else if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD)
         *launches = 5;
     else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
         *launches = la::tc_causal_launches();
@@ -229,10 +231,14 @@ la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void*
                       workspace_bytes, stream);
 }
 
-la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
-                        void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
-                        la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
-                        la_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+la_status backward(bool causal, const void* q, const void* k, const void* v, const void* dout,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                   la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                   la_stream_t stream) {
     la_status s = check_common(B, H, N, Dk, Dv, dt);
     if (s != LA_OK) return s;
     if ((s = check_eps(eps)) != LA_OK) return s;
@@ -245,11 +251,32 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
         (s = check_tensor(dv, rows * Dv, dt)))
         return s;
     if (rows == 0) return LA_OK;
-    const size_t need = kHeaderBytes + body_bytes(LA_OP_CAUSAL_BWD, B, H, N, Dk, Dv, dt);
+    const la_op op = causal ? LA_OP_CAUSAL_BWD : LA_OP_NONCAUSAL_BWD;
+    const size_t need = kHeaderBytes + body_bytes(op, B, H, N, Dk, Dv, dt);
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
-    return from_cuda(la::simt_causal_bwd(q, k, v, dout, dq, dk, dv, dt, BH, N, Dk, Dv, eps, body,
-                                         (cudaStream_t)stream));
+    return from_cuda(la::simt_bwd(q, k, v, dout, dq, dk, dv, dt, causal, BH, N, Dk, Dv, eps, body,
+                                  (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                        void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                        la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                        la_stream_t stream) {
+    return backward(true, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, eps, workspace,
+                    workspace_bytes, stream);
+}
+
+la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                           void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                           la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                           la_stream_t stream) {
+    return backward(false, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, eps, workspace,
+                    workspace_bytes, stream);
 }
 
 la_status la_decode_step(const void* q, const void* k, const void* v, void* o, float* S,

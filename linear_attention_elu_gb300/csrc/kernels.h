@@ -18,12 +18,13 @@ cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la
                         int64_t BH, int N, int D, int M, float eps, const float* S0,
                         const float* z0, float* S_out, float* z_out, void* scratch,
                         cudaStream_t st);
-// Causal backward (fp32 arithmetic, D, M <= kBwdMaxDim): dq, dk, dv from dout.
+// Causal or non-causal backward (fp32 arithmetic, D, M <= kBwdMaxDim): dq, dk,
+// dv from dout.
 constexpr int kBwdMaxDim = 64;
-size_t simt_causal_bwd_workspace(int64_t BH, int N, int D, int M);
-cudaError_t simt_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
-                            void* dq, void* dk, void* dv, la_dtype dt, int64_t BH, int N, int D,
-                            int M, float eps, void* scratch, cudaStream_t st);
+size_t simt_bwd_workspace(int64_t BH, int N, int D, int M);
+cudaError_t simt_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                     void* dk, void* dv, la_dtype dt, bool causal, int64_t BH, int N, int D, int M,
+                     float eps, void* scratch, cudaStream_t st);
 cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
                            int64_t BH, int N, int D, int M, float eps, void* scratch,
                            cudaStream_t st);

@@ -23,6 +23,7 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kScanBatch = 8;  // chunks per batch of loads in the chunk scans
 
 template <typename T>
 __device__ __forceinline__ void load_rows_phi(float* dst, int ld, const T* src, int rows,
@@ -88,10 +89,19 @@ __global__ void chunk_scan_kernel(float* __restrict__ states, const float* __res
     int e = (int)(gid - bh * E);
     float* p = states + bh * nchunks * (int64_t)E + e;
     float run = !S0 ? 0.f : e < D * M ? S0[bh * D * M + e] : z0[bh * D + (e - D * M)];
-    for (int c = 0; c < nchunks; ++c) {
-        float t = p[(int64_t)c * E];
-        p[(int64_t)c * E] = run;
-        run += t;
+    // Batches of kScanBatch chunks: all loads of a batch are in flight before
+    // its stores, instead of one DRAM round trip per chunk.
+    for (int c0 = 0; c0 < nchunks; c0 += kScanBatch) {
+        float t[kScanBatch];
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u)
+            t[u] = c0 + u < nchunks ? p[(int64_t)(c0 + u) * E] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u)
+            if (c0 + u < nchunks) {
+                p[(int64_t)(c0 + u) * E] = run;
+                run += t[u];
+            }
     }
     if (e < D * M) {
         if (S_out) S_out[bh * D * M + e] = run;
@@ -322,87 +332,217 @@ cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, voi
 // the chunk's carried-in state and a masked in-chunk part, as in the forward.
 // dq = dphi(q) * phi'(q) with phi'(x) = 1 (x > 0), e^x (x <= 0) = min(phi(x), 1).
 
-// grid (nchunks, BH): per row dnum (M) and dden into rowg [BH, N, M + 1]; per
-// chunk [dR ; dr] = sum_i phi(q_i) [dnum_i ; dden_i]^T into rstates.
+// Register-tiled products on 64 x 64 fp32 tiles in shared memory, rows of kLd
+// floats. Thread t of 256 owns output rows 4 tr .. 4 tr + 3 (tr = t / 16) and
+// four columns: 4 tc .. 4 tc + 3 when the B operand is stored k-major, tc,
+// tc + 16, tc + 32, tc + 48 when it is stored column-major (tc = t % 16). Every
+// operand load is a float4 over four consecutive k (or four consecutive rows,
+// or columns); with rows of 68 floats none of them is bank-conflicted beyond
+// the two wavefronts a 16-lane float4 load needs. The 32 lanes of warp w own
+// rows 8 w .. 8 w + 7, which bounds the triangular sums warp-uniformly.
+constexpr int kLd = 68;
+
+__device__ __forceinline__ int col_of(bool b_kmajor, int tc, int y) {
+    return b_kmajor ? 4 * tc + y : tc + 16 * y;
+}
+
+// acc[x][y] += sum_{k0 <= k < k1} Aop(4 tr + x, k) Bop(k, col_of(y)), k0 and k1
+// multiples of 4. Aop(r, k) is A[r kLd + k] (row-major) or A[k kLd + r]
+// (k-major); Bop(k, c) is B[k kLd + c] (k-major) or B[c kLd + k] (column-major).
+template <bool kAKmaj, bool kBKmaj>
+__device__ __forceinline__ void mm4(float (&acc)[4][4], const float* A, const float* B, int k0,
+                                    int k1, int tr, int tc) {
+#pragma unroll 2
+    for (int kk = k0; kk < k1; kk += 4) {
+        float a[4][4], b[4][4];  // a[x][u] = Aop(r_x, kk + u), b[u][y] = Bop(kk + u, c_y)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (kAKmaj) {
+                const float4 f = *reinterpret_cast<const float4*>(A + (kk + i) * kLd + 4 * tr);
+                a[0][i] = f.x, a[1][i] = f.y, a[2][i] = f.z, a[3][i] = f.w;
+            } else {
+                const float4 f = *reinterpret_cast<const float4*>(A + (4 * tr + i) * kLd + kk);
+                a[i][0] = f.x, a[i][1] = f.y, a[i][2] = f.z, a[i][3] = f.w;
+            }
+            if (kBKmaj) {
+                const float4 f = *reinterpret_cast<const float4*>(B + (kk + i) * kLd + 4 * tc);
+                b[i][0] = f.x, b[i][1] = f.y, b[i][2] = f.z, b[i][3] = f.w;
+            } else {
+                const float4 f = *reinterpret_cast<const float4*>(B + (tc + 16 * i) * kLd + kk);
+                b[0][i] = f.x, b[1][i] = f.y, b[2][i] = f.z, b[3][i] = f.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x][u], b[u][y], acc[x][y]);
+    }
+}
+
+__device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+}
+
+// A [64][width] global tile into shared rows of kLd floats (phi applied when
+// `with_phi`); rows >= valid and columns >= width are zero. The trip count is
+// fixed so that each thread's 16 loads are in flight together.
+constexpr int kPerThread = kChunk * kChunk / kThreads;
 template <typename T>
-__global__ void __launch_bounds__(kThreads) bwd_rows_kernel(
+__device__ __forceinline__ void load_tile(float* dst, const T* src, int valid, int width,
+                                          bool with_phi) {
+    float x[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads, r = idx >> 6, c = idx & 63;
+        x[u] = (r < valid && c < width) ? to_f(src[(int64_t)r * width + c]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads, r = idx >> 6, c = idx & 63;
+        dst[r * kLd + c] = (with_phi && r < valid && c < width) ? phi(x[u]) : x[u];
+    }
+}
+
+// A [D][M] state block into shared memory, as stored (dst[d kLd + m]) or
+// transposed (dst[m kLd + d]); entries beyond D or M are zero.
+__device__ __forceinline__ void load_state(float* dst, const float* src, int D, int M,
+                                           bool transposed) {
+    float x[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads, d = idx >> 6, m = idx & 63;
+        x[u] = (d < D && m < M) ? src[d * M + m] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads, d = idx >> 6, m = idx & 63;
+        dst[transposed ? m * kLd + d : d * kLd + m] = x[u];
+    }
+}
+
+// The chunk's dnum rows of rowg ([64][M + 1] from row 0) into shared rows.
+__device__ __forceinline__ void load_dnum(float* dst, const float* rg, int valid, int M) {
+    float x[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads, r = idx >> 6, c = idx & 63;
+        x[u] = (r < valid && c < M) ? rg[(int64_t)r * (M + 1) + c] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int idx = threadIdx.x + u * kThreads;
+        dst[(idx >> 6) * kLd + (idx & 63)] = x[u];
+    }
+}
+
+// grid (nchunks, BH): per row dnum (M) and dden into rowg [BH, N, M + 1]; per
+// chunk [dR ; dr] = sum_i phi(q_i) [dnum_i ; dden_i]^T into rstates. Causal:
+// the chunk's slot of `states` holds its carried-in state and the rows add the
+// masked in-chunk part; non-causal: chunk 0's slot holds the whole sequence's
+// (S, z), which every row sees.
+template <typename T, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 2) bwd_rows_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ dout, const float* __restrict__ states, float* __restrict__ rowg,
     float* __restrict__ rstates, int N, int D, int M, float eps) {
-    extern __shared__ float sm[];
-    const int ldk = D + 1;
-    float* fQ = sm;                       // [64][D+1]
-    float* fK = fQ + kChunk * ldk;        // [64][D+1]
-    float* sV = fK + kChunk * ldk;        // [64][M]
-    float* sG = sV + kChunk * M;          // [64][M]   g, then dnum
-    float* P = sG + kChunk * M;           // [D][M] then zP [D]
-    float* A = P + D * M + D;             // [64][65]
-    float* den = A + kChunk * (kChunk + 1);   // [64]
-    float* dd = den + kChunk;                 // [64] dden
+    extern __shared__ __align__(16) float sm[];
+    float* fQ = sm;                       // [64][kLd] each
+    float* fK = fQ + kChunk * kLd;
+    float* sV = fK + kChunk * kLd;
+    float* sG = sV + kChunk * kLd;        // g, then dnum
+    float* P = sG + kChunk * kLd;         // S_prev [d][m]
+    float* A = P + kChunk * kLd;          // phi(q_i).phi(k_j), j <= i
+    float* zP = A + kChunk * kLd;         // [64]
+    float* den = zP + kChunk;             // [64]
+    float* dot = den + kChunk;            // [64]
+    float* dd = dot + kChunk;             // [64]
     const int c = blockIdx.x, nchunks = gridDim.x;
     const int64_t bh = blockIdx.y;
     const int t0 = c * kChunk;
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
-    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
-    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D);
-    load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
-    load_rows(sG, M, dout + (bh * N + t0) * M, kChunk, valid, M);
-    const float* st = states + (bh * nchunks + c) * (int64_t)E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) P[e] = st[e];
-    __syncthreads();
-    const float* zP = P + D * M;
-    for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += blockDim.x) {
-        int i = idx >> 6, j = idx & 63;
-        float s = 0.f;
-        if (j <= i && i < valid)
-            for (int cc = 0; cc < D; ++cc) s = fmaf(fQ[i * ldk + cc], fK[j * ldk + cc], s);
-        A[i * (kChunk + 1) + j] = s;
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    if (kCausal) {
+        load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
+        load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
     }
+    load_tile(sG, dout + (bh * N + t0) * M, valid, M, false);
+    const float* st = states + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
+    load_state(P, st, D, M, false);
+    for (int idx = t; idx < kChunk; idx += blockDim.x) zP[idx] = idx < D ? st[D * M + idx] : 0.f;
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < kChunk; i += kThreads / 32) {
-        float s = A[i * (kChunk + 1) + lane] + A[i * (kChunk + 1) + lane + 32];
-        for (int cc = lane; cc < D; cc += 32) s = fmaf(fQ[i * ldk + cc], zP[cc], s);
+    float acc[4][4];
+    if (kCausal) {
+        // A = phi(Q) phi(K)^T, masked to j <= i.
+        zero4x4(acc);
+        mm4<false, false>(acc, fQ, fK, 0, kChunk, tr, tc);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) den[i] = s + eps;
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                const int i = 4 * tr + x, j = col_of(false, tc, y);
+                A[i * kLd + j] = j <= i ? acc[x][y] : 0.f;
+            }
+        __syncthreads();
+    }
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float s2 = kCausal ? A[i * kLd + lane] + A[i * kLd + lane + 32] : 0.f;
+        for (int cc = lane; cc < D; cc += 32) s2 = fmaf(fQ[i * kLd + cc], zP[cc], s2);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        if (lane == 0) den[i] = s2 + eps;
     }
     __syncthreads();
-    // o_i (recomputed) -> dnum_i = g_i / den_i and the row dot g_i . o_i, one warp per row.
+    // num = A V + phi(Q) S_prev; o = num / den; dnum = g / den; row dots g . o.
+    // A(i, j) is zero for j > i: the sum over j stops after the warp's last row.
+    zero4x4(acc);
+    if (kCausal) mm4<false, true>(acc, A, sV, 0, 8 * warp + 8, tr, tc);
+    mm4<false, true>(acc, fQ, P, 0, kChunk, tr, tc);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int i = 4 * tr + x;
+        float part = 0.f;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int m = col_of(true, tc, y);
+            const float g = sG[i * kLd + m];
+            part = fmaf(g, acc[x][y] / den[i], part);
+            sG[i * kLd + m] = (i < valid && m < M) ? g / den[i] : 0.f;
+        }
+        // The 16 lanes with the same tr share row i.
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (tc == 0) dot[i] = part;
+    }
+    __syncthreads();
+    for (int i = t; i < kChunk; i += blockDim.x) dd[i] = i < valid ? -dot[i] / den[i] : 0.f;
+    __syncthreads();
     float* rg = rowg + (bh * N + t0) * (int64_t)(M + 1);
-    for (int i = warp; i < kChunk; i += kThreads / 32) {
-        float dot = 0.f;
-        for (int m = lane; m < M; m += 32) {
-            float s = 0.f;
-            for (int j = 0; j <= i; ++j) s = fmaf(A[i * (kChunk + 1) + j], sV[j * M + m], s);
-            for (int cc = 0; cc < D; ++cc) s = fmaf(fQ[i * ldk + cc], P[cc * M + m], s);
-            const float o = s / den[i];
-            const float g = sG[i * M + m];
-            dot = fmaf(g, o, dot);
-            sG[i * M + m] = g / den[i];                   // dnum (a row is owned by one warp)
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        const float ddn = -dot / den[i];
-        if (lane == 0) dd[i] = i < valid ? ddn : 0.f;
-        if (i < valid) {
-            for (int m = lane; m < M; m += 32) rg[(int64_t)i * (M + 1) + m] = sG[i * M + m];
-            if (lane == 0) rg[(int64_t)i * (M + 1) + M] = ddn;
-        }
+    for (int idx = t; idx < valid * (M + 1); idx += blockDim.x) {
+        const int i = idx / (M + 1), m = idx - i * (M + 1);
+        rg[idx] = m < M ? sG[i * kLd + m] : dd[i];
     }
-    __syncthreads();
+    // dR = phi(Q)^T dnum (rows d, columns m); dr = phi(Q)^T dden.
     float* out = rstates + (bh * nchunks + c) * (int64_t)E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float s = 0.f;
-        if (e < D * M) {
-            int cc = e / M, m = e - cc * M;
-            for (int i = 0; i < valid; ++i) s = fmaf(fQ[i * ldk + cc], sG[i * M + m], s);
-        } else {
-            int cc = e - D * M;
-            for (int i = 0; i < valid; ++i) s = fmaf(fQ[i * ldk + cc], dd[i], s);
+    zero4x4(acc);
+    mm4<true, true>(acc, fQ, sG, 0, kChunk, tr, tc);
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int d = 4 * tr + x, m = col_of(true, tc, y);
+            if (d < D && m < M) out[d * M + m] = acc[x][y];
         }
-        out[e] = s;
+    for (int d = t; d < D; d += blockDim.x) {
+        float s2 = 0.f;
+        for (int i = 0; i < valid; ++i) s2 = fmaf(fQ[i * kLd + d], dd[i], s2);
+        out[D * M + d] = s2;
     }
 }
 
@@ -414,133 +554,223 @@ __global__ void chunk_rscan_kernel(float* __restrict__ rstates, int64_t BH, int 
     int e = (int)(gid - bh * E);
     float* p = rstates + bh * nchunks * (int64_t)E + e;
     float run = 0.f;
-    for (int c = nchunks - 1; c >= 0; --c) {
-        float t = p[(int64_t)c * E];
-        p[(int64_t)c * E] = run;
-        run += t;
+    for (int c0 = nchunks - 1; c0 >= 0; c0 -= kScanBatch) {
+        float t[kScanBatch];
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) t[u] = c0 - u >= 0 ? p[(int64_t)(c0 - u) * E] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u)
+            if (c0 - u >= 0) {
+                p[(int64_t)(c0 - u) * E] = run;
+                run += t[u];
+            }
+    }
+}
+
+// Sum over chunks, in place: chunk 0 of each (bh) gets the sum of all chunks.
+__global__ void chunk_total_kernel(float* __restrict__ parts, int64_t BH, int nchunks, int E) {
+    int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= BH * E) return;
+    int64_t bh = gid / E;
+    int e = (int)(gid - bh * E);
+    float* p = parts + bh * nchunks * (int64_t)E + e;
+    float run = 0.f;
+    for (int c0 = 0; c0 < nchunks; c0 += kScanBatch) {
+        float t[kScanBatch];
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) t[u] = c0 + u < nchunks ? p[(int64_t)(c0 + u) * E] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u)
+            if (c0 + u < nchunks) run += t[u];
+    }
+    p[0] = run;
+}
+
+// grid (nchunks, BH), D, M <= 64: the chunk's [S ; z] = phi(K)^T [V | 1] into
+// states [BH, nchunks, D*M + D].
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_state_kernel(const T* __restrict__ k,
+                                                             const T* __restrict__ v,
+                                                             float* __restrict__ states, int N,
+                                                             int D, int M) {
+    extern __shared__ __align__(16) float sm[];
+    float* fK = sm;                       // [64][kLd]
+    float* sV = fK + kChunk * kLd;
+    const int c = blockIdx.x, nchunks = gridDim.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * kChunk;
+    const int valid = min(kChunk, N - t0);
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15;
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+    __syncthreads();
+    float* out = states + (bh * nchunks + c) * (int64_t)(D * M + D);
+    float acc[4][4];
+    zero4x4(acc);
+    mm4<true, true>(acc, fK, sV, 0, kChunk, tr, tc);
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int d = 4 * tr + x, m = col_of(true, tc, y);
+            if (d < D && m < M) out[d * M + m] = acc[x][y];
+        }
+    if (t < D) {
+        float s2 = 0.f;
+        for (int j = 0; j < kChunk; ++j) s2 += fK[j * kLd + t];
+        out[D * M + t] = s2;
     }
 }
 
 // grid (nchunks, BH): dq, dk, dv of the chunk from its carried-in forward state
 // (S_prev, z_prev), the carried-in reverse sums (R_next, r_next) and the rows'
-// dnum, dden.
-template <typename T>
+// dnum, dden. Non-causal: chunk 0's slots hold the whole sequence's (S, z) and
+// (R, r), and there are no in-chunk terms.
+template <typename T, bool kCausal>
 __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ states, const float* __restrict__ rstates,
     const float* __restrict__ rowg, T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv,
     int N, int D, int M) {
-    extern __shared__ float sm[];
-    const int ldk = D + 1;
-    float* fQ = sm;                       // [64][D+1]
-    float* fK = fQ + kChunk * ldk;        // [64][D+1]
-    float* sV = fK + kChunk * ldk;        // [64][M]
-    float* DN = sV + kChunk * M;          // [64][M] dnum
-    float* dd = DN + kChunk * M;          // [64] dden
-    float* P = dd + kChunk;               // [D][M] S_prev, then z_prev [D]
-    float* R = P + D * M + D;             // [D][M] R_next, then r_next [D]
-    float* W = R + D * M + D;             // [64][65] phi(q_i).phi(k_j), j <= i
-    float* G = W + kChunk * (kChunk + 1); // [64][65] v_j.dnum_i + dden_i, j <= i
+    extern __shared__ __align__(16) float sm[];
+    float* fQ = sm;                       // [64][kLd] each
+    float* fK = fQ + kChunk * kLd;
+    float* sV = fK + kChunk * kLd;
+    float* DN = sV + kChunk * kLd;        // dnum [i][m]
+    float* G = DN + kChunk * kLd;         // v_j.dnum_i + dden_i, j <= i
+    float* PW = G + kChunk * kLd;         // S_prev^T [m][d], then W = phi(q_i).phi(k_j), j <= i
+    float* R = PW + kChunk * kLd;         // R_next [d][m]
+    float* Rt = R + kChunk * kLd;         // R_next^T [m][d]
+    float* dd = Rt + kChunk * kLd;        // [64]
+    float* zP = dd + kChunk;              // [64]
+    float* rr = zP + kChunk;              // [64]
     const int c = blockIdx.x, nchunks = gridDim.x;
     const int64_t bh = blockIdx.y;
     const int t0 = c * kChunk;
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
-    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
-    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D);
-    load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5;
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
     const float* rg = rowg + (bh * N + t0) * (int64_t)(M + 1);
-    for (int idx = threadIdx.x; idx < kChunk * (M + 1); idx += blockDim.x) {
-        int i = idx / (M + 1), m = idx - i * (M + 1);
-        float x = i < valid ? rg[idx] : 0.f;
-        if (m < M) DN[i * M + m] = x;
-        else dd[i] = x;
-    }
-    const float* st = states + (bh * nchunks + c) * (int64_t)E;
-    const float* rs = rstates + (bh * nchunks + c) * (int64_t)E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        P[e] = st[e];
-        R[e] = rs[e];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += blockDim.x) {
-        int i = idx >> 6, j = idx & 63;
-        float w = 0.f, g = 0.f;
-        if (j <= i && i < valid) {
-            for (int cc = 0; cc < D; ++cc) w = fmaf(fQ[i * ldk + cc], fK[j * ldk + cc], w);
-            for (int m = 0; m < M; ++m) g = fmaf(sV[j * M + m], DN[i * M + m], g);
-            g += dd[i];
-        }
-        W[i * (kChunk + 1) + j] = w;
-        G[i * (kChunk + 1) + j] = g;
+    const float* st = states + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
+    const float* rs = rstates + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
+    load_dnum(DN, rg, valid, M);
+    load_state(PW, st, D, M, true);
+    load_state(R, rs, D, M, false);
+    load_state(Rt, rs, D, M, true);
+    for (int idx = t; idx < kChunk; idx += blockDim.x) {
+        dd[idx] = idx < valid ? rg[(int64_t)idx * (M + 1) + M] : 0.f;
+        zP[idx] = idx < D ? st[D * M + idx] : 0.f;
+        rr[idx] = idx < D ? rs[D * M + idx] : 0.f;
     }
     __syncthreads();
-    // dq: dphi(q_i) = S_prev dnum_i + z_prev dden_i + sum_{j<=i} G_ij phi(k_j).
+    float acc[4][4];
+    if (kCausal) {
+        // G = dnum V^T + dden 1^T, masked to j <= i.
+        zero4x4(acc);
+        mm4<false, false>(acc, DN, sV, 0, kChunk, tr, tc);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                const int i = 4 * tr + x, j = col_of(false, tc, y);
+                G[i * kLd + j] = (j <= i && i < valid) ? acc[x][y] + dd[i] : 0.f;
+            }
+    }
+    __syncthreads();
+    // dphi(q) = dnum S_prev^T + dden z_prev^T + G phi(K); rows i, columns d.
+    zero4x4(acc);
+    mm4<false, true>(acc, DN, PW, 0, kChunk, tr, tc);
+    if (kCausal) mm4<false, true>(acc, G, fK, 0, 8 * warp + 8, tr, tc);
     T* dqc = dq + (bh * N + t0) * D;
-    for (int idx = threadIdx.x; idx < kChunk * D; idx += blockDim.x) {
-        int i = idx / D, d = idx - i * D;
-        if (i >= valid) continue;
-        float s = P[D * M + d] * dd[i];
-        for (int m = 0; m < M; ++m) s = fmaf(P[d * M + m], DN[i * M + m], s);
-        for (int j = 0; j <= i; ++j) s = fmaf(G[i * (kChunk + 1) + j], fK[j * ldk + d], s);
-        const float f = fQ[i * ldk + d];
-        dqc[(int64_t)i * D + d] = from_f<T>(s * fminf(f, 1.f));
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int i = 4 * tr + x, d = col_of(true, tc, y);
+            if (i < valid && d < D) {
+                const float s2 = fmaf(zP[d], dd[i], acc[x][y]);
+                dqc[(int64_t)i * D + d] = from_f<T>(s2 * fminf(fQ[i * kLd + d], 1.f));
+            }
+        }
+    if (kCausal) {
+        __syncthreads();  // S_prev^T is dead: its tile takes W
+        zero4x4(acc);
+        mm4<false, false>(acc, fQ, fK, 0, kChunk, tr, tc);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                const int i = 4 * tr + x, j = col_of(false, tc, y);
+                PW[i * kLd + j] = j <= i ? acc[x][y] : 0.f;
+            }
     }
-    // dk: dphi(k_j) = R_next v_j + r_next + sum_{i>=j} G_ij phi(q_i).
+    // dphi(k) = V R_next^T + r_next^T + G^T phi(Q); rows j, columns d. G(i, j) is
+    // zero for i < j: the sum over i starts at the warp's first row.
+    zero4x4(acc);
+    mm4<false, true>(acc, sV, Rt, 0, kChunk, tr, tc);
+    if (kCausal) mm4<true, true>(acc, G, fQ, 8 * warp, kChunk, tr, tc);
     T* dkc = dk + (bh * N + t0) * D;
-    for (int idx = threadIdx.x; idx < kChunk * D; idx += blockDim.x) {
-        int j = idx / D, d = idx - j * D;
-        if (j >= valid) continue;
-        float s = R[D * M + d];
-        for (int m = 0; m < M; ++m) s = fmaf(R[d * M + m], sV[j * M + m], s);
-        for (int i = j; i < valid; ++i) s = fmaf(G[i * (kChunk + 1) + j], fQ[i * ldk + d], s);
-        const float f = fK[j * ldk + d];
-        dkc[(int64_t)j * D + d] = from_f<T>(s * fminf(f, 1.f));
-    }
-    // dv: dv_j = R_next^T phi(k_j) + sum_{i>=j} W_ij dnum_i.
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int j = 4 * tr + x, d = col_of(true, tc, y);
+            if (j < valid && d < D)
+                dkc[(int64_t)j * D + d] = from_f<T>((acc[x][y] + rr[d]) * fminf(fK[j * kLd + d], 1.f));
+        }
+    if (kCausal) __syncthreads();
+    // dv = phi(K) R_next + W^T dnum; rows j, columns m.
+    zero4x4(acc);
+    mm4<false, true>(acc, fK, R, 0, kChunk, tr, tc);
+    if (kCausal) mm4<true, true>(acc, PW, DN, 8 * warp, kChunk, tr, tc);
     T* dvc = dv + (bh * N + t0) * M;
-    for (int idx = threadIdx.x; idx < kChunk * M; idx += blockDim.x) {
-        int j = idx / M, m = idx - j * M;
-        if (j >= valid) continue;
-        float s = 0.f;
-        for (int d = 0; d < D; ++d) s = fmaf(R[d * M + m], fK[j * ldk + d], s);
-        for (int i = j; i < valid; ++i) s = fmaf(W[i * (kChunk + 1) + j], DN[i * M + m], s);
-        dvc[(int64_t)j * M + m] = from_f<T>(s);
-    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int j = 4 * tr + x, m = col_of(true, tc, y);
+            if (j < valid && m < M) dvc[(int64_t)j * M + m] = from_f<T>(acc[x][y]);
+        }
 }
 
-template <typename T>
-cudaError_t simt_causal_bwd_impl(const void* q, const void* k, const void* v, const void* dout,
-                                 void* dq, void* dk, void* dv, int64_t BH, int N, int D, int M,
-                                 float eps, float* states, float* rstates, float* rowg,
-                                 cudaStream_t st) {
+template <typename T, bool kCausal>
+cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                          void* dk, void* dv, int64_t BH, int N, int D, int M, float eps,
+                          float* states, float* rstates, float* rowg, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     dim3 grid(nchunks, (unsigned)BH);
-    const size_t sm1 = sizeof(float) * (size_t)kChunk * (D + M);
-    const size_t sm2 = sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + 2 * M) + (size_t)D * M + D +
-                                        kChunk * (kChunk + 1) + 2 * kChunk);
-    const size_t sm3 = sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + 2 * M) + kChunk +
-                                        2 * ((size_t)D * M + D) + 2 * kChunk * (kChunk + 1));
+    const size_t sm1 = sizeof(float) * (2 * (size_t)kChunk * kLd);
+    const size_t sm2 = sizeof(float) * (6 * (size_t)kChunk * kLd + 4 * kChunk);
+    const size_t sm3 = sizeof(float) * (8 * (size_t)kChunk * kLd + 3 * kChunk);
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(chunk_state_kernel<T>,
+    if ((err = cudaFuncSetAttribute(bwd_state_kernel<T>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
-        (err = cudaFuncSetAttribute(bwd_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sm2)) ||
-        (err = cudaFuncSetAttribute(bwd_grad_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sm3)))
+        (err = cudaFuncSetAttribute(bwd_rows_kernel<T, kCausal>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) ||
+        (err = cudaFuncSetAttribute(bwd_grad_kernel<T, kCausal>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
         return err;
     const int E = D * M + D;
     const int64_t total = BH * (int64_t)E;
-    chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
-    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, nullptr, nullptr,
-                                                                        nullptr, nullptr, BH,
-                                                                        nchunks, D, M);
-    bwd_rows_kernel<T><<<grid, kThreads, sm2, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                                    (const T*)dout, states, rowg, rstates, N, D,
-                                                    M, eps);
-    chunk_rscan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(rstates, BH, nchunks, E);
-    bwd_grad_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v, states,
-                                                    rstates, rowg, (T*)dq, (T*)dk, (T*)dv, N, D, M);
+    const unsigned sgrid = (unsigned)((total + 255) / 256);
+    bwd_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
+    if (kCausal)
+        chunk_scan_kernel<<<sgrid, 256, 0, st>>>(states, nullptr, nullptr, nullptr, nullptr, BH,
+                                                 nchunks, D, M);
+    else
+        chunk_total_kernel<<<sgrid, 256, 0, st>>>(states, BH, nchunks, E);
+    bwd_rows_kernel<T, kCausal><<<grid, kThreads, sm2, st>>>(
+        (const T*)q, (const T*)k, (const T*)v, (const T*)dout, states, rowg, rstates, N, D, M, eps);
+    if (kCausal)
+        chunk_rscan_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
+    else
+        chunk_total_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
+    bwd_grad_kernel<T, kCausal><<<grid, kThreads, sm3, st>>>(
+        (const T*)q, (const T*)k, (const T*)v, states, rstates, rowg, (T*)dq, (T*)dk, (T*)dv, N, D,
+        M);
     return cudaPeekAtLastError();
 }
 
@@ -590,24 +820,28 @@ cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o,
                                               total, st);
 }
 
-size_t simt_causal_bwd_workspace(int64_t BH, int N, int D, int M) {
+size_t simt_bwd_workspace(int64_t BH, int N, int D, int M) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     return sizeof(float) * ((size_t)2 * BH * nchunks * (size_t)(D * M + D) +
                             (size_t)BH * N * (size_t)(M + 1));
 }
 
-cudaError_t simt_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
-                            void* dq, void* dk, void* dv, la_dtype dt, int64_t BH, int N, int D,
-                            int M, float eps, void* scratch, cudaStream_t st) {
+cudaError_t simt_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                     void* dk, void* dv, la_dtype dt, bool causal, int64_t BH, int N, int D, int M,
+                     float eps, void* scratch, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     float* states = (float*)scratch;
     float* rstates = states + (size_t)BH * nchunks * (size_t)(D * M + D);
     float* rowg = rstates + (size_t)BH * nchunks * (size_t)(D * M + D);
     if (dt == LA_F32)
-        return simt_causal_bwd_impl<float>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, states,
-                                           rstates, rowg, st);
-    return simt_causal_bwd_impl<__nv_bfloat16>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, states,
-                                               rstates, rowg, st);
+        return causal ? simt_bwd_impl<float, true>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+                                                   states, rstates, rowg, st)
+                      : simt_bwd_impl<float, false>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+                                                    states, rstates, rowg, st);
+    return causal ? simt_bwd_impl<__nv_bfloat16, true>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+                                                       states, rstates, rowg, st)
+                  : simt_bwd_impl<__nv_bfloat16, false>(q, k, v, dout, dq, dk, dv, BH, N, D, M,
+                                                        eps, states, rstates, rowg, st);
 }
 
 }  // namespace la

@@ -56,6 +56,21 @@ def test_workspace_size(lib):
         assert lib.la_workspace_size(op, 8, 8, 0, 64, 64, lib.LA_BF16) == 256
 
 
+def test_backward_workspace_and_launches(lib):
+    # Both backward directions use the same scratch: per-chunk forward and reverse
+    # sums (B*H*ceil(N/64)*(Dk*Dv + Dk) floats each) and per-row (dnum, dden)
+    # (B*H*N*(Dv + 1) floats), after the 256-byte header.
+    B, H, N, D = 8, 8, 3072, 64
+    body = 4 * (2 * B * H * (N // 64) * (D * D + D) + B * H * N * (D + 1))
+    for op in (lib.LA_OP_CAUSAL_BWD, lib.LA_OP_NONCAUSAL_BWD):
+        assert lib.la_workspace_size(op, B, H, N, D, D, lib.LA_BF16) == 256 + (body + 255) // 256 * 256
+        assert lib.la_launch_count(op, B, H, N, D, D, lib.LA_BF16) == 5
+        assert lib.la_launch_count(op, B, H, 0, D, D, lib.LA_BF16) == 0
+    so = ctypes.CDLL(lib.library_path())
+    n = ctypes.c_size_t(0)
+    assert so.la_workspace_size(lib.LA_OP_NONCAUSAL_BWD, 1, 1, 64, 128, 64, 1, ctypes.byref(n)) == 2
+
+
 def _raw(lib):
     return ctypes.CDLL(lib.library_path())
 

@@ -1,4 +1,5 @@
-"""la_causal_bwd against the float64 gradient oracle (oracle/backward.py).
+"""la_causal_bwd and la_noncausal_bwd against the float64 gradient oracle
+(oracle/backward.py).
 
 Gate, per gradient tensor and head: max |gpu - oracle| / max |oracle| over the
 head's [N, D] gradient, with 1e-4 for float32 inputs and 2e-2 for bfloat16
@@ -50,26 +51,71 @@ def test_gradients_match_oracle(la, B, H, N, D, M, dt):
         assert err <= TOL[dt], (name, err)
 
 
+@pytest.mark.parametrize("B,H,N,D,M,dt", [
+    (1, 1, 5, 3, 2, "f32"),          # shorter than a chunk, odd widths
+    (2, 2, 200, 64, 64, "f32"),      # several chunks, ragged tail
+    (1, 3, 130, 32, 48, "f32"),      # Dk != Dv
+    (2, 2, 333, 64, 64, "bf16"),     # bf16 inputs and gradients
+    (1, 2, 2500, 64, 64, "bf16"),    # 40 chunks summed into the totals
+])
+def test_noncausal_gradients_match_oracle(la, B, H, N, D, M, dt):
+    q, k, v = make_qkv(B, H, N, D, dt, seed=N + D + 7, Dv=M)
+    g = make_qkv(B, H, N, M, dt, seed=N + D + 8)[2]
+    dev = torch.device("cuda")
+    dq, dk, dv = la.la_noncausal_bwd(q.to(dev), k.to(dev), v.to(dev), g.to(dev))
+    torch.cuda.synchronize()
+    rq, rk, rv = bwd.grads(to_f64(q), to_f64(k), to_f64(v), to_f64(g), False)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = headwise_rel(to_f64(got), ref)
+        assert err <= TOL[dt], (name, err)
+
+
+def test_noncausal_loss_on_first_row_reaches_every_token(la):
+    # Without the mask, row 0 depends on every key and value: dv_j = R^T phi(k_j)
+    # with R = phi(q_0) dnum_0^T is nonzero for every j.
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 100, 64, "f32", seed=6))
+    g = torch.zeros_like(v)
+    g[0, 0, 0] = torch.randn(64, device="cuda")
+    dq, dk, dv = la.la_noncausal_bwd(q, k, v, g)
+    torch.cuda.synchronize()
+    assert float(dq[0, 0, 1:].abs().max()) == 0
+    assert bool((dv[0, 0].abs().amax(-1) > 0).all())
+
+
 def test_zero_upstream_gradient_gives_zero(la):
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 150, 64, "f32", seed=3))
-    dq, dk, dv = la.la_causal_bwd(q, k, v, torch.zeros_like(v))
-    torch.cuda.synchronize()
-    assert float(dq.abs().max()) == 0 and float(dk.abs().max()) == 0 and float(dv.abs().max()) == 0
+    for fn in (la.la_causal_bwd, la.la_noncausal_bwd):
+        dq, dk, dv = fn(q, k, v, torch.zeros_like(v))
+        torch.cuda.synchronize()
+        assert float(dq.abs().max()) == 0 and float(dk.abs().max()) == 0 and float(dv.abs().max()) == 0
 
 
 def test_loss_on_first_row_only_touches_first_token(la):
-    # Causality: a loss on row 0 alone reaches token 0 only.
+    # Causality: a loss on row 0 alone reaches token 0 only, exactly. There
+    # o_0 = v_0 w / (w + eps) with w = phi(q_0).phi(k_0), so dv_0 = g_0 w / (w + eps)
+    # in closed form, while dq_0 and dk_0 carry the factor g_0 . (v_0 - o_0), of
+    # order eps / w: compared with the oracle in absolute terms only.
     q, k, v = (t.cuda() for t in make_qkv(1, 1, 100, 64, "f32", seed=4))
     g = torch.zeros_like(v)
     g[0, 0, 0] = torch.randn(64, device="cuda")
     dq, dk, dv = la.la_causal_bwd(q, k, v, g)
     torch.cuda.synchronize()
     for t in (dq, dk, dv):
-        assert float(t[0, 0, 1:].abs().max()) == 0 and float(t[0, 0, 0].abs().max()) > 0
+        assert float(t[0, 0, 1:].abs().max()) == 0
+    fq, fk = (np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0))) for x in
+              (to_f64(q)[0, 0, 0], to_f64(k)[0, 0, 0]))
+    w = float(fq @ fk)
+    g0 = to_f64(g)[0, 0, 0]
+    np.testing.assert_allclose(to_f64(dv)[0, 0, 0], g0 * w / (w + 1e-6), rtol=1e-5, atol=1e-7)
+    rq, rk, _ = bwd.grads(to_f64(q), to_f64(k), to_f64(v), to_f64(g), True)
+    scale = np.abs(g0).max()
+    assert np.abs(to_f64(dq)[0, 0, 0] - rq[0, 0, 0]).max() <= 1e-5 * scale
+    assert np.abs(to_f64(dk)[0, 0, 0] - rk[0, 0, 0]).max() <= 1e-5 * scale
 
 
 def test_wide_heads_are_refused(la):
     q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 128, "bf16", seed=5))
-    with pytest.raises(la.LinAttnError) as e:
-        la.la_causal_bwd(q, k, v, torch.zeros_like(v))
-    assert e.value.status == 2  # LA_ERR_UNSUPPORTED
+    for fn in (la.la_causal_bwd, la.la_noncausal_bwd):
+        with pytest.raises(la.LinAttnError) as e:
+            fn(q, k, v, torch.zeros_like(v))
+        assert e.value.status == 2  # LA_ERR_UNSUPPORTED
