@@ -246,6 +246,9 @@ def run_reference(args, w):
 # 4,160; rows 8,320 (den 64, num 4,096, reverse sum 4,160); gradients 12,352
 # (dq 4,096 + 64, dk 4,096, dv 4,096).
 BWD_MACS_PER_TOKEN_D64 = 4160 + 12513 + 24832
+# The fp32 causal forward per token at Dk = Dv = 64: chunk state 4,160; output
+# A 2,080, den 64, A V 2,080, phi(q) S_prev 4,096.
+FWD_F32_MACS_PER_TOKEN_D64 = 4160 + 2080 + 64 + 2080 + 4096
 NC_BWD_MACS_PER_TOKEN_D64 = 4160 + 8320 + 12352
 # fp32 FMA peak from the unit counts and clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz.
 FP32_FMA_PEAK = 152 * 128 * 2 * 2.07e9
@@ -317,9 +320,35 @@ def other_paths(la, dev, stream):
                      "frac_of_hbm": per_step / (us * 1e-6) / 1e9 / hbm,
                      "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
     del q, k, v, o, S, z, g
+    # Causal forward on fp32 inputs (the fp32 SIMT path) at the image shape
+    # B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
+    w = WORKLOADS["image"]
+    q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen) for _ in range(3))
+    o = torch.empty_like(v)
+    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
+    la.la_causal_fwd(q, k, v, o=o, ws=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        la.la_causal_fwd(q, k, v, o=o, ws=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 10
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    flops = w.tokens * 2 * FWD_F32_MACS_PER_TOKEN_D64
+    out["causal_f32"] = {"workload": w.name.replace("bf16", "f32"),
+                         "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+                         "tflops": flops / (ms * 1e-3) / 1e12,
+                         "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
+                         "bound": "alu (fp32 FMA)"}
+    del q, k, v, o, ws, g
     # Causal and non-causal backward (fp32 SIMT arithmetic) at the image shape
     # B=8 H=8 N=3072 D=64 bf16.
-    w = WORKLOADS["image"]
     q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
                      for _ in range(4))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

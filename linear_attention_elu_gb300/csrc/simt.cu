@@ -267,30 +267,6 @@ __global__ void __launch_bounds__(kThreads) nc_apply_kernel(const T* __restrict_
     }
 }
 
-template <typename T>
-cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* o, int64_t BH,
-                             int N, int D, int M, float eps, const float* S0, const float* z0,
-                             float* S_out, float* z_out, float* states, cudaStream_t st) {
-    const int nchunks = (N + kChunk - 1) / kChunk;
-    dim3 grid(nchunks, (unsigned)BH);
-    size_t sm1 = sizeof(float) * (size_t)kChunk * (D + M);
-    size_t sm3 = sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + M) + (size_t)D * M + D +
-                                  kChunk * (kChunk + 1) + kChunk);
-    cudaError_t err;
-    if ((err = cudaFuncSetAttribute(chunk_state_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
-        return err;
-    if ((err = cudaFuncSetAttribute(chunk_output_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
-        return err;
-    chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
-    const int64_t total = BH * (int64_t)(D * M + D);
-    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, S0, z0, S_out,
-                                                                        z_out, BH, nchunks, D, M);
-    chunk_output_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                                        states, (T*)o, N, D, M, eps);
-    return cudaPeekAtLastError();
-}
 
 template <typename T>
 cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, void* o,
@@ -589,7 +565,7 @@ __global__ void chunk_total_kernel(float* __restrict__ parts, int64_t BH, int nc
 // grid (nchunks, BH), D, M <= 64: the chunk's [S ; z] = phi(K)^T [V | 1] into
 // states [BH, nchunks, D*M + D].
 template <typename T>
-__global__ void __launch_bounds__(kThreads) bwd_state_kernel(const T* __restrict__ k,
+__global__ void __launch_bounds__(kThreads) chunk_state_tiled_kernel(const T* __restrict__ k,
                                                              const T* __restrict__ v,
                                                              float* __restrict__ states, int N,
                                                              int D, int M) {
@@ -736,6 +712,110 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
         }
 }
 
+// grid (nchunks, BH), D, M <= 64: the chunk's rows of the causal output from
+// its exclusive prefix state (S_prev, z_prev) and the masked in-chunk terms,
+// o_i = (sum_{j <= i} A_ij v_j + phi(q_i)^T S_prev) / (sum_{j <= i} A_ij +
+// phi(q_i)^T z_prev + eps) with A_ij = phi(q_i).phi(k_j). Register-tiled; the
+// same sums in the same order as chunk_output_kernel.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) chunk_output_tiled_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const float* __restrict__ states, T* __restrict__ o, int N, int D, int M, float eps) {
+    extern __shared__ __align__(16) float sm[];
+    float* fQ = sm;                       // [64][kLd] each
+    float* fK = fQ + kChunk * kLd;
+    float* sV = fK + kChunk * kLd;
+    float* P = sV + kChunk * kLd;         // S_prev [d][m]
+    float* A = P + kChunk * kLd;          // phi(q_i).phi(k_j), j <= i
+    float* zP = A + kChunk * kLd;         // [64]
+    float* den = zP + kChunk;             // [64]
+    const int c = blockIdx.x, nchunks = gridDim.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * kChunk;
+    const int valid = min(kChunk, N - t0);
+    const int E = D * M + D;
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+    const float* st = states + (bh * nchunks + c) * (int64_t)E;
+    load_state(P, st, D, M, false);
+    for (int idx = t; idx < kChunk; idx += blockDim.x) zP[idx] = idx < D ? st[D * M + idx] : 0.f;
+    __syncthreads();
+    float acc[4][4];
+    zero4x4(acc);
+    mm4<false, false>(acc, fQ, fK, 0, kChunk, tr, tc);
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int i = 4 * tr + x, j = col_of(false, tc, y);
+            A[i * kLd + j] = (j <= i && i < valid) ? acc[x][y] : 0.f;
+        }
+    __syncthreads();
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float s2 = A[i * kLd + lane] + A[i * kLd + lane + 32];
+        for (int cc = lane; cc < D; cc += 32) s2 = fmaf(fQ[i * kLd + cc], zP[cc], s2);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        if (lane == 0) den[i] = s2 + eps;
+    }
+    __syncthreads();
+    zero4x4(acc);
+    mm4<false, true>(acc, A, sV, 0, 8 * warp + 8, tr, tc);
+    mm4<false, true>(acc, fQ, P, 0, kChunk, tr, tc);
+    T* oc = o + (bh * N + t0) * M;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int i = 4 * tr + x, m = col_of(true, tc, y);
+            if (i < valid && m < M) oc[(int64_t)i * M + m] = from_f<T>(acc[x][y] / den[i]);
+        }
+}
+
+template <typename T>
+cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* o, int64_t BH,
+                             int N, int D, int M, float eps, const float* S0, const float* z0,
+                             float* S_out, float* z_out, float* states, cudaStream_t st) {
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    dim3 grid(nchunks, (unsigned)BH);
+    const bool tiled = D <= kChunk && M <= kChunk;
+    const size_t sm1 = tiled ? sizeof(float) * (2 * (size_t)kChunk * kLd)
+                             : sizeof(float) * (size_t)kChunk * (D + M);
+    const size_t sm3 = tiled ? sizeof(float) * (5 * (size_t)kChunk * kLd + 2 * kChunk)
+                             : sizeof(float) * ((size_t)kChunk * (2 * (D + 1) + M) +
+                                                (size_t)D * M + D + kChunk * (kChunk + 1) + kChunk);
+    cudaError_t err;
+    if (tiled) {
+        if ((err = cudaFuncSetAttribute(chunk_state_tiled_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
+            (err = cudaFuncSetAttribute(chunk_output_tiled_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
+            return err;
+        chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states,
+                                                                 N, D, M);
+    } else {
+        if ((err = cudaFuncSetAttribute(chunk_state_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
+            (err = cudaFuncSetAttribute(chunk_output_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
+            return err;
+        chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D,
+                                                           M);
+    }
+    const int64_t total = BH * (int64_t)(D * M + D);
+    chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, S0, z0, S_out,
+                                                                        z_out, BH, nchunks, D, M);
+    if (tiled)
+        chunk_output_tiled_kernel<T><<<grid, kThreads, sm3, st>>>(
+            (const T*)q, (const T*)k, (const T*)v, states, (T*)o, N, D, M, eps);
+    else
+        chunk_output_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v,
+                                                            states, (T*)o, N, D, M, eps);
+    return cudaPeekAtLastError();
+}
+
 template <typename T, bool kCausal>
 cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const void* dout, void* dq,
                           void* dk, void* dv, int64_t BH, int N, int D, int M, float eps,
@@ -746,7 +826,7 @@ cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const voi
     const size_t sm2 = sizeof(float) * (6 * (size_t)kChunk * kLd + 4 * kChunk);
     const size_t sm3 = sizeof(float) * (8 * (size_t)kChunk * kLd + 3 * kChunk);
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(bwd_state_kernel<T>,
+    if ((err = cudaFuncSetAttribute(chunk_state_tiled_kernel<T>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
         (err = cudaFuncSetAttribute(bwd_rows_kernel<T, kCausal>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) ||
@@ -756,7 +836,7 @@ cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const voi
     const int E = D * M + D;
     const int64_t total = BH * (int64_t)E;
     const unsigned sgrid = (unsigned)((total + 255) / 256);
-    bwd_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
+    chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
     if (kCausal)
         chunk_scan_kernel<<<sgrid, 256, 0, st>>>(states, nullptr, nullptr, nullptr, nullptr, BH,
                                                  nchunks, D, M);
