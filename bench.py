@@ -249,6 +249,8 @@ BWD_MACS_PER_TOKEN_D64 = 4160 + 12513 + 24832
 # The fp32 causal forward per token at Dk = Dv = 64: chunk state 4,160; output
 # A 2,080, den 64, A V 2,080, phi(q) S_prev 4,096.
 FWD_F32_MACS_PER_TOKEN_D64 = 4160 + 2080 + 64 + 2080 + 4096
+# The fp32 non-causal forward per token: partial state 4,160; den 64, phi(q) S 4,096.
+NC_F32_MACS_PER_TOKEN_D64 = 4160 + 64 + 4096
 NC_BWD_MACS_PER_TOKEN_D64 = 4160 + 8320 + 12352
 # fp32 FMA peak from the unit counts and clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz.
 FP32_FMA_PEAK = 152 * 128 * 2 * 2.07e9
@@ -320,33 +322,38 @@ def other_paths(la, dev, stream):
                      "frac_of_hbm": per_step / (us * 1e-6) / 1e9 / hbm,
                      "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
     del q, k, v, o, S, z, g
-    # Causal forward on fp32 inputs (the fp32 SIMT path) at the image shape
-    # B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
+    # Causal and non-causal forward on fp32 inputs (the fp32 SIMT path) at the
+    # image shape B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
     w = WORKLOADS["image"]
     q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen) for _ in range(3))
     o = torch.empty_like(v)
-    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
-    la.la_causal_fwd(q, k, v, o=o, ws=ws)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        la.la_causal_fwd(q, k, v, o=o, ws=ws)
-    g.replay()
-    torch.cuda.synchronize()
-    reps = 10
-    a.record(stream)
-    for _ in range(reps):
+    for key, fn, op, macs, name in (
+            ("causal_f32", la.la_causal_fwd, la.LA_OP_CAUSAL, FWD_F32_MACS_PER_TOKEN_D64,
+             w.name.replace("bf16", "f32")),
+            ("noncausal_f32", la.la_noncausal_fwd, la.LA_OP_NONCAUSAL, NC_F32_MACS_PER_TOKEN_D64,
+             w.name.replace("bf16", "f32").replace("causal", "non-causal"))):
+        ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
+        fn(q, k, v, o=o, ws=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(q, k, v, o=o, ws=ws)
         g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
-    flops = w.tokens * 2 * FWD_F32_MACS_PER_TOKEN_D64
-    out["causal_f32"] = {"workload": w.name.replace("bf16", "f32"),
-                         "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
-                         "tflops": flops / (ms * 1e-3) / 1e12,
-                         "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
-                         "bound": "alu (fp32 FMA)"}
-    del q, k, v, o, ws, g
+        torch.cuda.synchronize()
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        flops = w.tokens * 2 * macs
+        out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+                    "ms_per_call": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
+                    "bound": "alu (fp32 FMA)"}
+        del ws, g
+    del q, k, v, o
     # Causal and non-causal backward (fp32 SIMT arithmetic) at the image shape
     # B=8 H=8 N=3072 D=64 bf16.
     q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()

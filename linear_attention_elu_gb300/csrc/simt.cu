@@ -268,31 +268,6 @@ __global__ void __launch_bounds__(kThreads) nc_apply_kernel(const T* __restrict_
 }
 
 
-template <typename T>
-cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, void* o,
-                                int64_t BH, int N, int D, int M, float eps, int nsplit,
-                                float* partials, float* total, cudaStream_t st) {
-    const int nchunks = (N + kChunk - 1) / kChunk;
-    const int per_split = ((nchunks + nsplit - 1) / nsplit) * kChunk;
-    size_t sm1 = sizeof(float) * (size_t)kChunk * (D + M);
-    size_t sm3 = sizeof(float) * ((size_t)kChunk * (D + 1) + (size_t)D * M + D + kChunk);
-    cudaError_t err;
-    if ((err = cudaFuncSetAttribute(nc_partial_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)))
-        return err;
-    if ((err = cudaFuncSetAttribute(nc_apply_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
-        return err;
-    nc_partial_kernel<T><<<dim3(nsplit, (unsigned)BH), kThreads, sm1, st>>>(
-        (const T*)k, (const T*)v, partials, N, D, M, per_split);
-    const int E = D * M + D;
-    const int64_t tot = BH * (int64_t)E;
-    nc_reduce_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(partials, total, BH, nsplit,
-                                                                     E);
-    nc_apply_kernel<T><<<dim3(nchunks, (unsigned)BH), kThreads, sm3, st>>>(
-        (const T*)q, total, (T*)o, N, D, M, eps);
-    return cudaPeekAtLastError();
-}
 
 // ------------------------------------------------------------ causal backward
 //
@@ -813,6 +788,133 @@ cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* 
     else
         chunk_output_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v,
                                                             states, (T*)o, N, D, M, eps);
+    return cudaPeekAtLastError();
+}
+
+// grid (nsplit, BH), D, M <= 64: partial [S ; z] over a contiguous token range,
+// register-tiled; the same sums in the same order as nc_partial_kernel.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) nc_partial_tiled_kernel(const T* __restrict__ k,
+                                                                    const T* __restrict__ v,
+                                                                    float* __restrict__ partials,
+                                                                    int N, int D, int M,
+                                                                    int tokens_per_split) {
+    extern __shared__ __align__(16) float sm[];
+    float* fK = sm;                       // [64][kLd]
+    float* sV = fK + kChunk * kLd;
+    const int s = blockIdx.x, nsplit = gridDim.x;
+    const int64_t bh = blockIdx.y;
+    const int E = D * M + D;
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15;
+    float acc[4][4];
+    zero4x4(acc);
+    float zacc = 0.f;
+    const int begin = s * tokens_per_split;
+    const int end = min(N, begin + tokens_per_split);
+    for (int t0 = begin; t0 < end; t0 += kChunk) {
+        const int valid = min(kChunk, end - t0);
+        __syncthreads();
+        load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
+        load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+        __syncthreads();
+        mm4<true, true>(acc, fK, sV, 0, kChunk, tr, tc);
+        if (t < D)
+            for (int j = 0; j < kChunk; ++j) zacc += fK[j * kLd + t];
+    }
+    float* out = partials + (bh * nsplit + s) * (int64_t)E;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int d = 4 * tr + x, m = col_of(true, tc, y);
+            if (d < D && m < M) out[d * M + m] = acc[x][y];
+        }
+    if (t < D) out[D * M + t] = zacc;
+}
+
+// grid (ceil(N/64), BH), D, M <= 64: o_i = phi(q_i)^T S / (phi(q_i)^T z + eps),
+// register-tiled; the same sums in the same order as nc_apply_kernel.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) nc_apply_tiled_kernel(const T* __restrict__ q,
+                                                                  const float* __restrict__ total,
+                                                                  T* __restrict__ o, int N, int D,
+                                                                  int M, float eps) {
+    extern __shared__ __align__(16) float sm[];
+    float* fQ = sm;                       // [64][kLd]
+    float* S = fQ + kChunk * kLd;         // [d][m]
+    float* z = S + kChunk * kLd;          // [64]
+    float* den = z + kChunk;              // [64]
+    const int64_t bh = blockIdx.y;
+    const int t0 = blockIdx.x * kChunk;
+    const int valid = min(kChunk, N - t0);
+    const int E = D * M + D;
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    const float* st = total + bh * E;
+    load_state(S, st, D, M, false);
+    for (int idx = t; idx < kChunk; idx += blockDim.x) z[idx] = idx < D ? st[D * M + idx] : 0.f;
+    __syncthreads();
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float s2 = 0.f;
+        for (int cc = lane; cc < D; cc += 32) s2 = fmaf(fQ[i * kLd + cc], z[cc], s2);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        if (lane == 0) den[i] = s2 + eps;
+    }
+    __syncthreads();
+    float acc[4][4];
+    zero4x4(acc);
+    mm4<false, true>(acc, fQ, S, 0, kChunk, tr, tc);
+    T* oc = o + (bh * N + t0) * M;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int i = 4 * tr + x, m = col_of(true, tc, y);
+            if (i < valid && m < M) oc[(int64_t)i * M + m] = from_f<T>(acc[x][y] / den[i]);
+        }
+}
+
+template <typename T>
+cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, void* o,
+                                int64_t BH, int N, int D, int M, float eps, int nsplit,
+                                float* partials, float* total, cudaStream_t st) {
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    const int per_split = ((nchunks + nsplit - 1) / nsplit) * kChunk;
+    const bool tiled = D <= kChunk && M <= kChunk;
+    const size_t sm1 = tiled ? sizeof(float) * (2 * (size_t)kChunk * kLd)
+                             : sizeof(float) * (size_t)kChunk * (D + M);
+    const size_t sm3 = tiled ? sizeof(float) * (2 * (size_t)kChunk * kLd + 2 * kChunk)
+                             : sizeof(float) * ((size_t)kChunk * (D + 1) + (size_t)D * M + D +
+                                                kChunk);
+    cudaError_t err;
+    if (tiled) {
+        if ((err = cudaFuncSetAttribute(nc_partial_tiled_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
+            (err = cudaFuncSetAttribute(nc_apply_tiled_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
+            return err;
+        nc_partial_tiled_kernel<T><<<dim3(nsplit, (unsigned)BH), kThreads, sm1, st>>>(
+            (const T*)k, (const T*)v, partials, N, D, M, per_split);
+    } else {
+        if ((err = cudaFuncSetAttribute(nc_partial_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
+            (err = cudaFuncSetAttribute(nc_apply_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
+            return err;
+        nc_partial_kernel<T><<<dim3(nsplit, (unsigned)BH), kThreads, sm1, st>>>(
+            (const T*)k, (const T*)v, partials, N, D, M, per_split);
+    }
+    const int E = D * M + D;
+    const int64_t tot = BH * (int64_t)E;
+    nc_reduce_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(partials, total, BH, nsplit,
+                                                                     E);
+    if (tiled)
+        nc_apply_tiled_kernel<T><<<dim3(nchunks, (unsigned)BH), kThreads, sm3, st>>>(
+            (const T*)q, total, (T*)o, N, D, M, eps);
+    else
+        nc_apply_kernel<T><<<dim3(nchunks, (unsigned)BH), kThreads, sm3, st>>>(
+            (const T*)q, total, (T*)o, N, D, M, eps);
     return cudaPeekAtLastError();
 }
 
