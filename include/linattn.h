@@ -74,6 +74,17 @@ typedef enum {
     LA_OP_NONCAUSAL_BWD = 4
 } la_op;
 
+/*
+ * The feature map phi the kernels apply to q and k. The method leaves phi free
+ * ("Why Replace Attention? The Softmax Bottleneck and the Path to Linear Time",
+ * section 4.5: any map into a feature space of its own width). LA_PHI_ELU1 is
+ * elu(x) + 1, the map of every entry without a `phi` argument; LA_PHI_IDENTITY
+ * applies none, for features the caller has already computed (for example with
+ * la_positive_random_features), whose width is then Dk. Features should be
+ * non-negative so that the denominators stay positive; nothing checks it.
+ */
+typedef enum { LA_PHI_ELU1 = 0, LA_PHI_IDENTITY = 1 } la_phi;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status s);
 
@@ -254,6 +265,51 @@ la_status la_causal_fwd_host(const void* q, const void* k, const void* v, void* 
 la_status la_decode_step(const void* q, const void* k, const void* v, void* o,
                          float* S, float* z, int B, int H, int Dk, int Dv, la_dtype dt,
                          float eps, la_stream_t stream);
+
+/*
+ * The entries above with the feature map as an argument (LA_ERR_INVALID_ARG for
+ * any other value). Same shapes, dtypes, workspaces, paths and errors as the
+ * entry of the same name without `_phi`; la_causal_fwd_phi also takes the
+ * optional initial state of la_causal_fwd_state. The backward entries multiply
+ * by the map's derivative: min(phi(x), 1) for elu + 1, 1 for the identity.
+ */
+la_status la_noncausal_fwd_phi(const void* q, const void* k, const void* v, void* o,
+                               int B, int H, int N, int Dk, int Dv, la_dtype dt, la_phi phi,
+                               float eps, void* workspace, size_t workspace_bytes,
+                               la_stream_t stream);
+la_status la_causal_fwd_phi(const void* q, const void* k, const void* v, void* o,
+                            int B, int H, int N, int Dk, int Dv, la_dtype dt, la_phi phi,
+                            float eps, const float* S0, const float* z0, float* S_out,
+                            float* z_out, void* workspace, size_t workspace_bytes,
+                            la_stream_t stream);
+la_status la_decode_step_phi(const void* q, const void* k, const void* v, void* o,
+                             float* S, float* z, int B, int H, int Dk, int Dv, la_dtype dt,
+                             la_phi phi, float eps, la_stream_t stream);
+la_status la_causal_bwd_phi(const void* q, const void* k, const void* v, const void* dout,
+                            void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                            la_dtype dt, la_phi phi, float eps, void* workspace,
+                            size_t workspace_bytes, la_stream_t stream);
+la_status la_noncausal_bwd_phi(const void* q, const void* k, const void* v, const void* dout,
+                               void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                               la_dtype dt, la_phi phi, float eps, void* workspace,
+                               size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * Positive random features: out[i, r] = exp(w_r . x_i - |x_i|^2 / 2 - shift)
+ * / sqrt(R) for the rows w_r of W. With the entries of W drawn from N(0, 1)
+ * (by the caller), E[phi(x) . phi(y)] = exp(x . y): an unbiased estimate of
+ * the exponential (softmax) kernel, the positive random features the
+ * research-hub "Linear Attention" page names ("Key math / How it works").
+ * `shift` is subtracted in every exponent against overflow; one shift for all
+ * keys of a head, or any per query row, cancels in the attention output.
+ *  - x: [rows, D], W: [R, D], out: [rows, R], all dtype dt, device pointers,
+ *    16-byte aligned; fp32 arithmetic. 1 <= D <= 128, 1 <= R <= 65535 * 64.
+ *  - The result feeds the *_phi entries with LA_PHI_IDENTITY and Dk = R.
+ *  - Needs no workspace; asynchronous on `stream`.
+ */
+la_status la_positive_random_features(const void* x, const void* W, void* out, int64_t rows,
+                                      int D, int R, la_dtype dt, float shift,
+                                      la_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the workspace status word.

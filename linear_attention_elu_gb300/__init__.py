@@ -22,11 +22,12 @@ __all__ = [
     "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
     "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
     "la_causal_bwd", "LA_OP_CAUSAL_BWD", "la_noncausal_bwd", "LA_OP_NONCAUSAL_BWD",
-    "library_path",
+    "LA_PHI_ELU1", "LA_PHI_IDENTITY", "la_positive_random_features", "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
 LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_BWD = 0, 1, 2, 3, 4
+LA_PHI_ELU1, LA_PHI_IDENTITY = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 
 _DTYPES = {torch.float32: LA_F32, torch.bfloat16: LA_BF16}
@@ -76,6 +77,19 @@ def _load():
     lib.la_causal_fwd_host.restype = I
     lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
     lib.la_decode_step.restype = I
+    L = ctypes.c_int64
+    lib.la_noncausal_fwd_phi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
+    lib.la_noncausal_fwd_phi.restype = I
+    lib.la_causal_fwd_phi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, P, Z, P]
+    lib.la_causal_fwd_phi.restype = I
+    lib.la_decode_step_phi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.la_decode_step_phi.restype = I
+    lib.la_causal_bwd_phi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
+    lib.la_causal_bwd_phi.restype = I
+    lib.la_noncausal_bwd_phi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
+    lib.la_noncausal_bwd_phi.restype = I
+    lib.la_positive_random_features.argtypes = [P, P, P, L, I, I, I, F, P]
+    lib.la_positive_random_features.restype = I
     lib.la_query_status.argtypes = [P, P]
     lib.la_query_status.restype = I
     return lib
@@ -162,22 +176,33 @@ def _shape4(q, k, v):
     return B, H, N, Dk, v.shape[3]
 
 
-def la_noncausal_fwd(q, k, v, o=None, eps=1e-6, ws=None, stream=None):
-    """o_i = phi(q_i)^T S / (phi(q_i)^T z + eps), S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j)."""
+def la_noncausal_fwd(q, k, v, o=None, eps=1e-6, ws=None, stream=None, phi=LA_PHI_ELU1):
+    """o_i = phi(q_i)^T S / (phi(q_i)^T z + eps), S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j).
+
+    `phi`: LA_PHI_ELU1 (elu + 1) or LA_PHI_IDENTITY (q, k are features already)."""
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if o is None:
         o = torch.empty_like(v)
     _need_cuda(q, k, v, o, ws)
     if ws is None:
         ws = workspace(LA_OP_NONCAUSAL, B, H, N, Dk, Dv, q.dtype, q.device, stream)
-    _check(_lib.la_noncausal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
-                                 float(eps), _ptr(ws), ws.numel(), _stream(stream)),
-           "la_noncausal_fwd")
+    if phi == LA_PHI_ELU1:
+        _check(_lib.la_noncausal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                                     float(eps), _ptr(ws), ws.numel(), _stream(stream)),
+               "la_noncausal_fwd")
+    else:
+        _check(_lib.la_noncausal_fwd_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv,
+                                         _dt(q), int(phi), float(eps), _ptr(ws), ws.numel(),
+                                         _stream(stream)),
+               "la_noncausal_fwd_phi")
     return o
 
 
-def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, stream=None):
+def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, stream=None,
+                  phi=LA_PHI_ELU1):
     """Causal o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i + eps); optional final state out (fp32)."""
+    if phi != LA_PHI_ELU1:
+        return _causal_phi(q, k, v, None, None, o, eps, S_out, z_out, ws, stream, phi)
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if o is None:
         o = torch.empty_like(v)
@@ -194,9 +219,29 @@ def la_causal_fwd(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, ws=None, st
     return o
 
 
+def _causal_phi(q, k, v, S0, z0, o, eps, S_out, z_out, ws, stream, phi):
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, ws, S0, z0, S_out, z_out)
+    for t, shp in ((S0, (B, H, Dk, Dv)), (z0, (B, H, Dk)), (S_out, (B, H, Dk, Dv)),
+                   (z_out, (B, H, Dk))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
+            raise ValueError(f"states must be float32 with shape {shp}")
+    if ws is None:
+        ws = workspace(LA_OP_CAUSAL, B, H, N, Dk, Dv, q.dtype, q.device, stream)
+    _check(_lib.la_causal_fwd_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv, _dt(q),
+                                  int(phi), float(eps), _ptr(S0), _ptr(z0), _ptr(S_out),
+                                  _ptr(z_out), _ptr(ws), ws.numel(), _stream(stream)),
+           "la_causal_fwd_phi")
+    return o
+
+
 def la_causal_fwd_state(q, k, v, S0, z0, o=None, eps=1e-6, S_out=None, z_out=None, ws=None,
-                        stream=None):
+                        stream=None, phi=LA_PHI_ELU1):
     """Causal forward continuing from the state (S0 [B,H,Dk,Dv], z0 [B,H,Dk], float32)."""
+    if phi != LA_PHI_ELU1:
+        return _causal_phi(q, k, v, S0, z0, o, eps, S_out, z_out, ws, stream, phi)
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if o is None:
         o = torch.empty_like(v)
@@ -214,7 +259,7 @@ def la_causal_fwd_state(q, k, v, S0, z0, o=None, eps=1e-6, S_out=None, z_out=Non
     return o
 
 
-def _bwd(fn, op, q, k, v, dout, dq, dk, dv, eps, ws, stream):
+def _bwd(fn, op, q, k, v, dout, dq, dk, dv, eps, ws, stream, phi=LA_PHI_ELU1):
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if dout.shape != v.shape or dout.dtype != v.dtype:
         raise ValueError("dout must be shaped and typed like v")
@@ -224,22 +269,31 @@ def _bwd(fn, op, q, k, v, dout, dq, dk, dv, eps, ws, stream):
     _need_cuda(q, k, v, dout, dq, dk, dv, ws)
     if ws is None:
         ws = workspace(op, B, H, N, Dk, Dv, q.dtype, q.device, stream)
-    _check(getattr(_lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                             B, H, N, Dk, Dv, _dt(q), float(eps), _ptr(ws), ws.numel(),
-                             _stream(stream)),
-           fn)
+    if phi == LA_PHI_ELU1:
+        _check(getattr(_lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, N, Dk, Dv, _dt(q), float(eps), _ptr(ws),
+                                 ws.numel(), _stream(stream)),
+               fn)
+    else:
+        _check(getattr(_lib, fn + "_phi")(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
+                                          _ptr(dk), _ptr(dv), B, H, N, Dk, Dv, _dt(q), int(phi),
+                                          float(eps), _ptr(ws), ws.numel(), _stream(stream)),
+               fn + "_phi")
     return dq, dk, dv
 
 
-def la_causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None):
+def la_causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None,
+                  phi=LA_PHI_ELU1):
     """Gradients (dq, dk, dv) of sum(o * dout) for the causal forward o of (q, k, v)."""
-    return _bwd("la_causal_bwd", LA_OP_CAUSAL_BWD, q, k, v, dout, dq, dk, dv, eps, ws, stream)
+    return _bwd("la_causal_bwd", LA_OP_CAUSAL_BWD, q, k, v, dout, dq, dk, dv, eps, ws, stream,
+                phi)
 
 
-def la_noncausal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None):
+def la_noncausal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, eps=1e-6, ws=None, stream=None,
+                     phi=LA_PHI_ELU1):
     """Gradients (dq, dk, dv) of sum(o * dout) for the non-causal forward o of (q, k, v)."""
     return _bwd("la_noncausal_bwd", LA_OP_NONCAUSAL_BWD, q, k, v, dout, dq, dk, dv, eps, ws,
-                stream)
+                stream, phi)
 
 
 def la_host_staging_size(B, H, N, Dk, Dv, dtype):
@@ -284,7 +338,7 @@ def la_causal_fwd_host(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, stagin
     return o
 
 
-def la_decode_step(q, k, v, S, z, o=None, eps=1e-6, stream=None):
+def la_decode_step(q, k, v, S, z, o=None, eps=1e-6, stream=None, phi=LA_PHI_ELU1):
     """One recurrent step on (S, z) in place; q, k [B,H,Dk], v [B,H,Dv]; returns o [B,H,Dv]."""
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
         raise ValueError("expected q, k [B,H,Dk] and v [B,H,Dv]")
@@ -296,10 +350,32 @@ def la_decode_step(q, k, v, S, z, o=None, eps=1e-6, stream=None):
     if o is None:
         o = torch.empty_like(v)
     _need_cuda(q, k, v, o, S, z)
-    _check(_lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H, Dk,
-                               Dv, _dt(q), float(eps), _stream(stream)),
-           "la_decode_step")
+    if phi == LA_PHI_ELU1:
+        _check(_lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H, Dk,
+                                   Dv, _dt(q), float(eps), _stream(stream)),
+               "la_decode_step")
+    else:
+        _check(_lib.la_decode_step_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H,
+                                       Dk, Dv, _dt(q), int(phi), float(eps), _stream(stream)),
+               "la_decode_step_phi")
     return o
+
+
+def la_positive_random_features(x, W, out=None, shift=0.0, stream=None):
+    """exp(W x - |x|^2 / 2 - shift) / sqrt(R) over the last axis of x [..., D]; W [R, D].
+
+    Returns out [..., R] in x's dtype: features for the LA_PHI_IDENTITY entries."""
+    if W.dim() != 2 or x.shape[-1] != W.shape[1] or W.dtype != x.dtype:
+        raise ValueError("expected x [..., D] and W [R, D] of one dtype")
+    R, D = W.shape
+    rows = x.numel() // D if D else 0
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (R,), dtype=x.dtype, device=x.device)
+    _need_cuda(x, W, out)
+    _check(_lib.la_positive_random_features(_ptr(x), _ptr(W), _ptr(out), rows, D, R, _dt(x),
+                                            float(shift), _stream(stream)),
+           "la_positive_random_features")
+    return out
 
 
 def la_query_status(ws, stream=None):

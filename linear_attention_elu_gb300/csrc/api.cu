@@ -75,13 +75,19 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
     return x < y + bn && y < x + an;
 }
 
+static_assert(LA_PHI_ELU1 == la::kPhiElu1 && LA_PHI_IDENTITY == la::kPhiIdentity,
+              "la_phi values are the kernels' feature-map codes");
+
+bool valid_phi(la_phi phi) { return phi == LA_PHI_ELU1 || phi == LA_PHI_IDENTITY; }
+
 la_status causal_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int N,
-                     int Dk, int Dv, la_dtype dt, float eps, const float* S0, const float* z0,
-                     float* S_out, float* z_out, void* workspace, size_t workspace_bytes,
-                     la_stream_t stream) {
+                     int Dk, int Dv, la_dtype dt, la_phi phi, float eps, const float* S0,
+                     const float* z0, float* S_out, float* z_out, void* workspace,
+                     size_t workspace_bytes, la_stream_t stream) {
     la_status s = check_common(B, H, N, Dk, Dv, dt);
     if (s != LA_OK) return s;
     if ((s = check_eps(eps)) != LA_OK) return s;
+    if (!valid_phi(phi)) return LA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     const int64_t rows = BH * N;
     if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
@@ -114,9 +120,9 @@ la_status causal_fwd(const void* q, const void* k, const void* v, void* o, int B
     char* body = (char*)workspace + kHeaderBytes;
     if (la::tc_causal_supported(Dk, Dv, dt))
         return from_cuda(
-            la::tc_causal(q, k, v, o, BH, N, eps, S0, z0, S_out, z_out, workspace, body, st));
-    return from_cuda(
-        la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, S0, z0, S_out, z_out, body, st));
+            la::tc_causal(q, k, v, o, BH, N, eps, phi, S0, z0, S_out, z_out, workspace, body, st));
+    return from_cuda(la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, phi, S0, z0, S_out, z_out,
+                                     body, st));
 }
 
 }  // namespace
@@ -196,9 +202,17 @@ la_status la_workspace_init(void* workspace, size_t workspace_bytes, la_stream_t
 la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
                            int N, int Dk, int Dv, la_dtype dt, float eps, void* workspace,
                            size_t workspace_bytes, la_stream_t stream) {
+    return la_noncausal_fwd_phi(q, k, v, o, B, H, N, Dk, Dv, dt, LA_PHI_ELU1, eps, workspace,
+                                workspace_bytes, stream);
+}
+
+la_status la_noncausal_fwd_phi(const void* q, const void* k, const void* v, void* o, int B,
+                               int H, int N, int Dk, int Dv, la_dtype dt, la_phi phi, float eps,
+                               void* workspace, size_t workspace_bytes, la_stream_t stream) {
     la_status s = check_common(B, H, N, Dk, Dv, dt);
     if (s != LA_OK) return s;
     if ((s = check_eps(eps)) != LA_OK) return s;
+    if (!valid_phi(phi)) return LA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     const int64_t rows = BH * N;
     if ((s = check_tensor(q, rows * Dk, dt)) || (s = check_tensor(k, rows * Dk, dt)) ||
@@ -209,9 +223,9 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
     if (la::tc_noncausal_supported(Dk, Dv, dt))
-        return from_cuda(la::tc_noncausal(q, k, v, o, BH, N, eps, workspace, body,
+        return from_cuda(la::tc_noncausal(q, k, v, o, BH, N, eps, phi, workspace, body,
                                           (cudaStream_t)stream));
-    return from_cuda(la::simt_noncausal(q, k, v, o, dt, BH, N, Dk, Dv, eps, body,
+    return from_cuda(la::simt_noncausal(q, k, v, o, dt, BH, N, Dk, Dv, eps, phi, body,
                                         (cudaStream_t)stream));
 }
 
@@ -219,15 +233,23 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, in
                         int N, int Dk, int Dv, la_dtype dt, float eps, float* S_out,
                         float* z_out, void* workspace, size_t workspace_bytes,
                         la_stream_t stream) {
-    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, eps, nullptr, nullptr, S_out, z_out,
-                      workspace, workspace_bytes, stream);
+    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, LA_PHI_ELU1, eps, nullptr, nullptr, S_out,
+                      z_out, workspace, workspace_bytes, stream);
 }
 
 la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void* o, int B,
                               int H, int N, int Dk, int Dv, la_dtype dt, float eps,
                               const float* S0, const float* z0, float* S_out, float* z_out,
                               void* workspace, size_t workspace_bytes, la_stream_t stream) {
-    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, eps, S0, z0, S_out, z_out, workspace,
+    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, LA_PHI_ELU1, eps, S0, z0, S_out, z_out,
+                      workspace, workspace_bytes, stream);
+}
+
+la_status la_causal_fwd_phi(const void* q, const void* k, const void* v, void* o, int B, int H,
+                            int N, int Dk, int Dv, la_dtype dt, la_phi phi, float eps,
+                            const float* S0, const float* z0, float* S_out, float* z_out,
+                            void* workspace, size_t workspace_bytes, la_stream_t stream) {
+    return causal_fwd(q, k, v, o, B, H, N, Dk, Dv, dt, phi, eps, S0, z0, S_out, z_out, workspace,
                       workspace_bytes, stream);
 }
 
@@ -237,11 +259,12 @@ namespace {
 
 la_status backward(bool causal, const void* q, const void* k, const void* v, const void* dout,
                    void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
-                   la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                   la_dtype dt, la_phi phi, float eps, void* workspace, size_t workspace_bytes,
                    la_stream_t stream) {
     la_status s = check_common(B, H, N, Dk, Dv, dt);
     if (s != LA_OK) return s;
     if ((s = check_eps(eps)) != LA_OK) return s;
+    if (!valid_phi(phi)) return LA_ERR_INVALID_ARG;
     if (Dk > la::kBwdMaxDim || Dv > la::kBwdMaxDim) return LA_ERR_UNSUPPORTED;
     const int64_t BH = (int64_t)B * H;
     const int64_t rows = BH * N;
@@ -255,8 +278,8 @@ la_status backward(bool causal, const void* q, const void* k, const void* v, con
     const size_t need = kHeaderBytes + body_bytes(op, B, H, N, Dk, Dv, dt);
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
-    return from_cuda(la::simt_bwd(q, k, v, dout, dq, dk, dv, dt, causal, BH, N, Dk, Dv, eps, body,
-                                  (cudaStream_t)stream));
+    return from_cuda(la::simt_bwd(q, k, v, dout, dq, dk, dv, dt, causal, BH, N, Dk, Dv, eps, phi,
+                                  body, (cudaStream_t)stream));
 }
 
 }  // namespace
@@ -267,7 +290,15 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
                         void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
                         la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
                         la_stream_t stream) {
-    return backward(true, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, eps, workspace,
+    return backward(true, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, LA_PHI_ELU1, eps,
+                    workspace, workspace_bytes, stream);
+}
+
+la_status la_causal_bwd_phi(const void* q, const void* k, const void* v, const void* dout,
+                            void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                            la_dtype dt, la_phi phi, float eps, void* workspace,
+                            size_t workspace_bytes, la_stream_t stream) {
+    return backward(true, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, phi, eps, workspace,
                     workspace_bytes, stream);
 }
 
@@ -275,23 +306,55 @@ la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const vo
                            void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
                            la_dtype dt, float eps, void* workspace, size_t workspace_bytes,
                            la_stream_t stream) {
-    return backward(false, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, eps, workspace,
+    return backward(false, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, LA_PHI_ELU1, eps,
+                    workspace, workspace_bytes, stream);
+}
+
+la_status la_noncausal_bwd_phi(const void* q, const void* k, const void* v, const void* dout,
+                               void* dq, void* dk, void* dv, int B, int H, int N, int Dk, int Dv,
+                               la_dtype dt, la_phi phi, float eps, void* workspace,
+                               size_t workspace_bytes, la_stream_t stream) {
+    return backward(false, q, k, v, dout, dq, dk, dv, B, H, N, Dk, Dv, dt, phi, eps, workspace,
                     workspace_bytes, stream);
 }
 
 la_status la_decode_step(const void* q, const void* k, const void* v, void* o, float* S,
                          float* z, int B, int H, int Dk, int Dv, la_dtype dt, float eps,
                          la_stream_t stream) {
+    return la_decode_step_phi(q, k, v, o, S, z, B, H, Dk, Dv, dt, LA_PHI_ELU1, eps, stream);
+}
+
+la_status la_decode_step_phi(const void* q, const void* k, const void* v, void* o, float* S,
+                             float* z, int B, int H, int Dk, int Dv, la_dtype dt, la_phi phi,
+                             float eps, la_stream_t stream) {
     la_status s = check_common(B, H, 1, Dk, Dv, dt);
     if (s != LA_OK) return s;
     if ((s = check_eps(eps)) != LA_OK) return s;
+    if (!valid_phi(phi)) return LA_ERR_INVALID_ARG;
     const int64_t BH = (int64_t)B * H;
     if (BH == 0) return LA_OK;
     if ((s = check_tensor(q, BH * Dk, dt)) || (s = check_tensor(k, BH * Dk, dt)) ||
         (s = check_tensor(v, BH * Dv, dt)) || (s = check_tensor(o, BH * Dv, dt)))
         return s;
     if (!S || !z || !aligned(S, 16) || !aligned(z, 4)) return LA_ERR_INVALID_ARG;
-    return from_cuda(la::decode_step(q, k, v, o, S, z, dt, BH, Dk, Dv, eps, (cudaStream_t)stream));
+    return from_cuda(
+        la::decode_step(q, k, v, o, S, z, dt, BH, Dk, Dv, eps, phi, (cudaStream_t)stream));
+}
+
+la_status la_positive_random_features(const void* x, const void* W, void* out, int64_t rows,
+                                      int D, int R, la_dtype dt, float shift,
+                                      la_stream_t stream) {
+    if (rows < 0 || D < 1 || D > la::kMaxDim || R < 1 || (int64_t)R > 65535LL * la::kChunk ||
+        (dt != LA_F32 && dt != LA_BF16) || !isfinite(shift))
+        return LA_ERR_INVALID_ARG;
+    if (rows == 0) return LA_OK;
+    if ((int64_t)((rows + la::kChunk - 1) / la::kChunk) > 2147483647LL) return LA_ERR_UNSUPPORTED;
+    la_status s;
+    if ((s = check_tensor(x, rows * D, dt)) || (s = check_tensor(W, (int64_t)R * D, dt)) ||
+        (s = check_tensor(out, rows * R, dt)))
+        return s;
+    return from_cuda(la::simt_random_features(x, W, out, dt, rows, D, R, shift,
+                                              (cudaStream_t)stream));
 }
 
 la_status la_query_status(void* workspace, la_stream_t stream) {

@@ -181,8 +181,10 @@ __device__ __forceinline__ float init_elem(const float* S0, const float* z0, int
 
 // kInit: the recurrence starts from (S0, z0) instead of zero. A separate
 // instantiation: the extra code costs the zero-start kernel several µs (this
-// kernel's timing is sensitive to code added anywhere in it).
-template <bool kInit>
+// kernel's timing is sensitive to code added anywhere in it). kPhi: the feature
+// map the phi role applies (elu + 1, or the identity for features computed by
+// the caller).
+template <bool kInit, int kPhi>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
@@ -384,7 +386,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int a = 0; a < nA && ok; ++a) {
             const int ch = (int)((last_start + a) % nchunks);
             ok = mbar_wait(&m.afull[a % kSlots], (a / kSlots) & 1, max_spin);
-            phi_tile_256(slot(a), t, min(kC, N - ch * kC));
+            phi_tile_256<kPhi>(slot(a), t, min(kC, N - ch * kC));
             fence_proxy_async_smem();
             ok = named_bar_and(kBarPhi, kPhiThreads, ok);
             if (ok && t == 0) mbar_arrive(&m.aphi[a % kSlots]);
@@ -395,7 +397,8 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             const int s = i % kStages;
             const int ch = (int)((u0 + i) % nchunks);
             if (ok) ok = mbar_wait(&m.full[s], (i / kStages) & 1, max_spin);
-            if (ok) phi_tiles2_256(stage(s) + kStK, min(kC, N - ch * kC), stage(s) + kStQ, kC, t);
+            if (ok)
+                phi_tiles2_256<kPhi>(stage(s) + kStK, min(kC, N - ch * kC), stage(s) + kStQ, kC, t);
             fence_proxy_async_smem();
             ok = named_bar_and(kBarPhi, kPhiThreads, ok);
             if (!ok) break;
@@ -819,8 +822,8 @@ size_t tc_causal_workspace(int64_t BH, int N) {
 int tc_causal_launches() { return 1; }
 
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, const float* S0, const float* z0, float* S_out, float* z_out,
-                      void* ws_header, void* scratch, cudaStream_t st) {
+                      float eps, int fm, const float* S0, const float* z0, float* S_out,
+                      float* z_out, void* ws_header, void* scratch, cudaStream_t st) {
     Partition p = make_partition(BH, N, grid_cap());
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     uint64_t* agg = reinterpret_cast<uint64_t*>(scratch);
@@ -830,10 +833,15 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    static std::atomic<int> optin[kMaxDevices], optin_init[kMaxDevices];
-    if ((err = S0 ? ensure_smem_optin(causal_fused_kernel<true>, (int)kSmem, optin_init)
-                  : ensure_smem_optin(causal_fused_kernel<false>, (int)kSmem, optin)))
-        return err;
+    // One instantiation per (initial state, feature map), each with its own opt-in flag.
+    using Kernel = decltype(&causal_fused_kernel<false, kPhiElu1>);
+    static std::atomic<int> optin[4][kMaxDevices];
+    const Kernel kernels[4] = {causal_fused_kernel<false, kPhiElu1>,
+                               causal_fused_kernel<true, kPhiElu1>,
+                               causal_fused_kernel<false, kPhiIdentity>,
+                               causal_fused_kernel<true, kPhiIdentity>};
+    const int variant = (S0 ? 1 : 0) + (fm == kPhiIdentity ? 2 : 0);
+    if ((err = ensure_smem_optin(kernels[variant], (int)kSmem, optin[variant]))) return err;
     // Programmatic stream serialization: the next call's CTAs may be scheduled on
     // SMs as this launch's CTAs finish and run their set-up; the kernel waits
     // (griddepcontrol.wait) before its first global-memory access.
@@ -847,9 +855,8 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, S0 ? causal_fused_kernel<true> : causal_fused_kernel<false>,
-                              qm, km, vm, om, agg, incl, S0, z0, S_out, z_out,
-                              p, N, eps, hdr);
+    return cudaLaunchKernelEx(&cfg, kernels[variant], qm, km, vm, om, agg, incl, S0, z0, S_out,
+                              z_out, p, N, eps, hdr);
 }
 
 }  // namespace la

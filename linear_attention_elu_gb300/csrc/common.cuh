@@ -18,6 +18,19 @@ constexpr int kChunk = 64;
 // Attention? The Softmax Bottleneck and the Path to Linear Time", section 5.3).
 __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
+// Feature maps (the values of la_phi in the C ABI): elu(x) + 1, or the identity
+// for features the caller has already computed -- the method leaves phi free
+// (same blog, section 4.5). kNoMap marks loads of values, which take no map.
+constexpr int kPhiElu1 = 0, kPhiIdentity = 1, kNoMap = -1;
+__device__ __forceinline__ float fmap(float x, int kind) {
+    return kind == kPhiIdentity ? x : phi(x);
+}
+// The map's derivative written through its value f = fmap(x): for elu(x) + 1,
+// 1 for x > 0 and e^x = f for x <= 0, i.e. min(f, 1); 1 for the identity.
+__device__ __forceinline__ float fmap_grad(float f, int kind) {
+    return kind == kPhiIdentity ? 1.f : fminf(f, 1.f);
+}
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 

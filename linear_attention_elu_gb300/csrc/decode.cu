@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(256) decode64_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ v,
                                                        T* __restrict__ o, float* __restrict__ S,
                                                        float* __restrict__ z, int64_t BH,
-                                                       float eps) {
+                                                       float eps, int fm) {
     const int lane = threadIdx.x & 31;
     const int64_t h = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (h >= BH) return;
@@ -31,8 +31,8 @@ __global__ void __launch_bounds__(256) decode64_kernel(const T* __restrict__ q,
     const T* kh = k + h * 64;
     const T* vh = v + h * 64;
     // Lane l holds phi(k), phi(q) and z for features l and l + 32.
-    const float fk0 = phi(to_f(kh[lane])), fk1 = phi(to_f(kh[lane + 32]));
-    const float fq0 = phi(to_f(qh[lane])), fq1 = phi(to_f(qh[lane + 32]));
+    const float fk0 = fmap(to_f(kh[lane]), fm), fk1 = fmap(to_f(kh[lane + 32]), fm);
+    const float fq0 = fmap(to_f(qh[lane]), fm), fq1 = fmap(to_f(qh[lane + 32]), fm);
     float* zh = z + h * 64;
     const float z0 = zh[lane] + fk0, z1 = zh[lane + 32] + fk1;
     zh[lane] = z0;
@@ -83,14 +83,15 @@ __global__ void __launch_bounds__(256) decode64_kernel(const T* __restrict__ q,
 template <typename T>
 __global__ void __launch_bounds__(128) decode_generic_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int D, int M, float eps) {
+    T* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int D, int M, float eps,
+    int fm) {
     __shared__ float fk[kMaxDim], fq[kMaxDim], red[4];
     const int64_t h = blockIdx.x;
     const int t = threadIdx.x;
     float dpart = 0.f;
     if (t < D) {
-        fk[t] = phi(to_f(k[h * D + t]));
-        fq[t] = phi(to_f(q[h * D + t]));
+        fk[t] = fmap(to_f(k[h * D + t]), fm);
+        fq[t] = fmap(to_f(q[h * D + t]), fm);
         float zn = z[h * D + t] + fk[t];
         z[h * D + t] = zn;
         dpart = fq[t] * zn;
@@ -115,16 +116,17 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(
 
 template <typename T>
 cudaError_t decode_impl(const void* q, const void* k, const void* v, void* o, float* S, float* z,
-                        int64_t BH, int D, int M, float eps, cudaStream_t st) {
+                        int64_t BH, int D, int M, float eps, int fm, cudaStream_t st) {
     if (D == 64 && M == 64) {
         const int heads_per_block = 8;
         const int64_t blocks = (BH + heads_per_block - 1) / heads_per_block;
         decode64_kernel<T><<<(unsigned)blocks, 256, 0, st>>>((const T*)q, (const T*)k,
-                                                             (const T*)v, (T*)o, S, z, BH, eps);
+                                                             (const T*)v, (T*)o, S, z, BH, eps,
+                                                             fm);
     } else {
         decode_generic_kernel<T><<<(unsigned)BH, 128, 0, st>>>((const T*)q, (const T*)k,
                                                                (const T*)v, (T*)o, S, z, D, M,
-                                                               eps);
+                                                               eps, fm);
     }
     return cudaPeekAtLastError();
 }
@@ -132,9 +134,10 @@ cudaError_t decode_impl(const void* q, const void* k, const void* v, void* o, fl
 }  // namespace
 
 cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,
-                        la_dtype dt, int64_t BH, int D, int M, float eps, cudaStream_t st) {
-    if (dt == LA_F32) return decode_impl<float>(q, k, v, o, S, z, BH, D, M, eps, st);
-    return decode_impl<__nv_bfloat16>(q, k, v, o, S, z, BH, D, M, eps, st);
+                        la_dtype dt, int64_t BH, int D, int M, float eps, int fm,
+                        cudaStream_t st) {
+    if (dt == LA_F32) return decode_impl<float>(q, k, v, o, S, z, BH, D, M, eps, fm, st);
+    return decode_impl<__nv_bfloat16>(q, k, v, o, S, z, BH, D, M, eps, fm, st);
 }
 
 }  // namespace la

@@ -9,13 +9,16 @@
 
 namespace la {
 
+// Every launcher takes `fm`, the feature map (the la_phi values: kPhiElu1 or
+// kPhiIdentity, defined in common.cuh).
+
 // fp32-arithmetic SIMT paths (any 1 <= D, M <= 128, either dtype).
 size_t simt_causal_workspace(int64_t BH, int N, int D, int M);
 size_t simt_noncausal_workspace(int64_t BH, int N, int D, int M);
 int simt_noncausal_splits(int64_t BH, int N);
 // S0, z0: initial state [BH, D, M] and [BH, D] (fp32, both or neither; null = zero).
 cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                        int64_t BH, int N, int D, int M, float eps, const float* S0,
+                        int64_t BH, int N, int D, int M, float eps, int fm, const float* S0,
                         const float* z0, float* S_out, float* z_out, void* scratch,
                         cudaStream_t st);
 // Causal or non-causal backward (fp32 arithmetic, D, M <= kBwdMaxDim): dq, dk,
@@ -24,27 +27,33 @@ constexpr int kBwdMaxDim = 64;
 size_t simt_bwd_workspace(int64_t BH, int N, int D, int M);
 cudaError_t simt_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq,
                      void* dk, void* dv, la_dtype dt, bool causal, int64_t BH, int N, int D, int M,
-                     float eps, void* scratch, cudaStream_t st);
+                     float eps, int fm, void* scratch, cudaStream_t st);
 cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                           int64_t BH, int N, int D, int M, float eps, void* scratch,
+                           int64_t BH, int N, int D, int M, float eps, int fm, void* scratch,
                            cudaStream_t st);
+
+// Positive random features exp(W x - |x|^2 / 2 - shift) / sqrt(R) (SIMT, fp32
+// arithmetic; D <= 128).
+cudaError_t simt_random_features(const void* x, const void* W, void* out, la_dtype dt,
+                                 int64_t rows, int D, int R, float shift, cudaStream_t st);
 
 // Tensor-core (tcgen05) causal path: bf16, Dk = Dv = 64.
 bool tc_causal_supported(int D, int M, la_dtype dt);
 size_t tc_causal_workspace(int64_t BH, int N);
 int tc_causal_launches();
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, const float* S0, const float* z0, float* S_out, float* z_out,
-                      void* ws_header, void* scratch, cudaStream_t st);
+                      float eps, int fm, const float* S0, const float* z0, float* S_out,
+                      float* z_out, void* ws_header, void* scratch, cudaStream_t st);
 
 // Tensor-core (tcgen05) non-causal path: bf16, Dk = Dv = 128.
 bool tc_noncausal_supported(int D, int M, la_dtype dt);
 size_t tc_noncausal_workspace(int64_t BH, int N);
 cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                         float eps, void* ws_header, void* scratch, cudaStream_t st);
+                         float eps, int fm, void* ws_header, void* scratch, cudaStream_t st);
 
 // Decode step (SIMT, bandwidth bound).
 cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,
-                        la_dtype dt, int64_t BH, int D, int M, float eps, cudaStream_t st);
+                        la_dtype dt, int64_t BH, int D, int M, float eps, int fm,
+                        cudaStream_t st);
 
 }  // namespace la

@@ -77,8 +77,9 @@ extern "C" la_status la_causal_fwd_noalloc(const void* q, const void* k, const v
     la_status s = scratch_for_current_device(st, &ws);
     if (s != LA_OK) return s;
     char* scratch = static_cast<char*>(ws) + kHeaderBytes;
-    cudaError_t err = tc ? la::tc_causal(q, k, v, o, BH, N, eps, nullptr, nullptr, S_out, z_out, ws, scratch, st)
-                         : la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, nullptr, nullptr, S_out, z_out,
-                                           scratch, st);
+    cudaError_t err = tc ? la::tc_causal(q, k, v, o, BH, N, eps, LA_PHI_ELU1, nullptr, nullptr, S_out,
+                                         z_out, ws, scratch, st)
+                         : la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, LA_PHI_ELU1, nullptr,
+                                           nullptr, S_out, z_out, scratch, st);
     return err == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }

@@ -46,6 +46,7 @@ constexpr uint32_t kSStage = 4 * kTileBytes;              // K0 K1 V0 V1 (64 KB)
 constexpr size_t kSSmem = 1024 + kSStages * kSStage;
 constexpr int kSThreads = 320;
 
+template <int kPhi>
 __global__ void __launch_bounds__(kSThreads, 1)
 nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 float* __restrict__ agg, Partition part, int N, WsHeader* hdr) {
@@ -174,7 +175,7 @@ nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     const int r = (t >> 3) + 32 * k;
                     uint4 o = make_uint4(0, 0, 0, 0);
                     if (r < valid) {
-                        o = phi8(v[k]);
+                        o = phi8<kPhi>(v[k]);
                         const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -261,13 +262,14 @@ constexpr uint32_t kTmStride = 256;                        // TMEM buffer b at 2
 
 // phi of row `row` of a 128 x 64 bf16 box (128-byte swizzle) into 32 TMEM
 // columns at taddr: the kind::f16 A-operand layout (two features per column).
+template <int kPhi>
 __device__ __forceinline__ void phi_row_to_tmem(const uint8_t* tile, uint32_t taddr, int row) {
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
         uint32_t w[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint4 x = phi8(*reinterpret_cast<const uint4*>(
+            const uint4 x = phi8<kPhi>(*reinterpret_cast<const uint4*>(
                 tile + row * 128 + (((4 * hlf + c) ^ (row & 7)) << 4)));
             w[4 * c] = x.x;
             w[4 * c + 1] = x.y;
@@ -286,6 +288,7 @@ struct ApplyMisc {
     uint32_t tmem_slot;
 };
 
+template <int kPhi>
 __global__ void __launch_bounds__(kAThreads, 1)
 nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                 const float* __restrict__ agg, Partition part, float eps, WsHeader* hdr) {
@@ -397,7 +400,7 @@ nc_apply_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             if (ok && i >= 2) ok = mbar_wait(&m.o_full[b], ((i - 2) >> 1) & 1, max_spin);
             tc_fence_after();
             if (ok)
-                phi_row_to_tmem(stage(s) + (warp >> 2) * kTileBytes,
+                phi_row_to_tmem<kPhi>(stage(s) + (warp >> 2) * kTileBytes,
                                 tmem + kTmStride * b + kTmQ + 32 * (warp >> 2) + lb, 32 * (warp & 3) + lane);
             tmem_st_wait();
             tc_fence_before();
@@ -535,7 +538,7 @@ size_t tc_noncausal_workspace(int64_t BH, int N) {
 }
 
 cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                         float eps, void* ws_header, void* scratch, cudaStream_t st) {
+                         float eps, int fm, void* ws_header, void* scratch, cudaStream_t st) {
     Partition p = make_partition(BH, N, sm_count());
     CUtensorMap qm, km, vm, om;
     if (!encode_bhnd(&qm, q, BH, N, kD) || !encode_bhnd(&km, k, BH, N, kD) ||
@@ -544,11 +547,14 @@ cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, i
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     float* agg = reinterpret_cast<float*>(scratch);
     cudaError_t err;
-    static std::atomic<int> optin_nc_state_kernel[kMaxDevices];
-    if ((err = ensure_smem_optin(nc_state_kernel, (int)kSSmem, optin_nc_state_kernel))) return err;
-    static std::atomic<int> optin_nc_apply_kernel[kMaxDevices];
-    if ((err = ensure_smem_optin(nc_apply_kernel, (int)kASmem, optin_nc_apply_kernel))) return err;
-    nc_state_kernel<<<p.grid, kSThreads, kSSmem, st>>>(km, vm, agg, p, N, hdr);
+    // One instantiation per feature map (elu + 1, identity), each with its own opt-in flag.
+    const bool ident = fm == kPhiIdentity;
+    auto state_kernel = ident ? nc_state_kernel<kPhiIdentity> : nc_state_kernel<kPhiElu1>;
+    auto apply_kernel = ident ? nc_apply_kernel<kPhiIdentity> : nc_apply_kernel<kPhiElu1>;
+    static std::atomic<int> optin_state[2][kMaxDevices], optin_apply[2][kMaxDevices];
+    if ((err = ensure_smem_optin(state_kernel, (int)kSSmem, optin_state[ident]))) return err;
+    if ((err = ensure_smem_optin(apply_kernel, (int)kASmem, optin_apply[ident]))) return err;
+    state_kernel<<<p.grid, kSThreads, kSSmem, st>>>(km, vm, agg, p, N, hdr);
     if ((err = cudaPeekAtLastError())) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
@@ -560,7 +566,7 @@ cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, nc_apply_kernel, qm, om, (const float*)agg, p, eps, hdr);
+    return cudaLaunchKernelEx(&cfg, apply_kernel, qm, om, (const float*)agg, p, eps, hdr);
 }
 
 }  // namespace la

@@ -27,11 +27,11 @@ constexpr int kScanBatch = 8;  // chunks per batch of loads in the chunk scans
 
 template <typename T>
 __device__ __forceinline__ void load_rows_phi(float* dst, int ld, const T* src, int rows,
-                                              int valid, int D) {
+                                              int valid, int D, int fm) {
     // dst[r * ld + c] = phi(src[r * D + c]) for r < valid, 0 for padded rows.
     for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
         int r = idx / D, c = idx - r * D;
-        dst[r * ld + c] = r < valid ? phi(to_f(src[(int64_t)r * D + c])) : 0.f;
+        dst[r * ld + c] = r < valid ? fmap(to_f(src[(int64_t)r * D + c]), fm) : 0.f;
     }
 }
 
@@ -49,7 +49,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const T* __restrict__ k,
                                                                const T* __restrict__ v,
                                                                float* __restrict__ states,
-                                                               int N, int D, int M) {
+                                                               int N, int D, int M, int fm) {
     extern __shared__ float sm[];
     float* fK = sm;                 // [64][D]
     float* sV = sm + kChunk * D;    // [64][M]
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const T* __restri
     const int64_t bh = blockIdx.y;
     const int t0 = c * kChunk;
     const int valid = min(kChunk, N - t0);
-    load_rows_phi(fK, D, k + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows_phi(fK, D, k + (bh * N + t0) * D, kChunk, valid, D, fm);
     load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
     __syncthreads();
     const int E = D * M + D;
@@ -114,7 +114,7 @@ __global__ void chunk_scan_kernel(float* __restrict__ states, const float* __res
 template <typename T>
 __global__ void __launch_bounds__(kThreads) chunk_output_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    const float* __restrict__ states, T* __restrict__ o, int N, int D, int M, float eps) {
+    const float* __restrict__ states, T* __restrict__ o, int N, int D, int M, float eps, int fm) {
     extern __shared__ float sm[];
     const int ldk = D + 1;
     float* fQ = sm;                       // [64][D+1]
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(
     const int t0 = c * kChunk;
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
-    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
-    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D, fm);
+    load_rows_phi(fK, ldk, k + (bh * N + t0) * D, kChunk, valid, D, fm);
     load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
     const float* st = states + (bh * nchunks + c) * (int64_t)E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) P[e] = st[e];
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) nc_partial_kernel(const T* __restric
                                                               const T* __restrict__ v,
                                                               float* __restrict__ partials,
                                                               int N, int D, int M,
-                                                              int tokens_per_split) {
+                                                              int tokens_per_split, int fm) {
     extern __shared__ float sm[];
     float* fK = sm;               // [64][D]
     float* sV = sm + kChunk * D;  // [64][M]
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) nc_partial_kernel(const T* __restric
     for (int t0 = begin; t0 < end; t0 += kChunk) {
         const int valid = min(kChunk, end - t0);
         __syncthreads();
-        load_rows_phi(fK, D, k + (bh * N + t0) * D, kChunk, valid, D);
+        load_rows_phi(fK, D, k + (bh * N + t0) * D, kChunk, valid, D, fm);
         load_rows(sV, M, v + (bh * N + t0) * M, kChunk, valid, M);
         __syncthreads();
 #pragma unroll
@@ -233,7 +233,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) nc_apply_kernel(const T* __restrict__ q,
                                                             const float* __restrict__ total,
                                                             T* __restrict__ o, int N, int D,
-                                                            int M, float eps) {
+                                                            int M, float eps, int fm) {
     extern __shared__ float sm[];
     const int ldk = D + 1;
     float* fQ = sm;                    // [64][D+1]
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) nc_apply_kernel(const T* __restrict_
     const int t0 = blockIdx.x * kChunk;
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
-    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D);
+    load_rows_phi(fQ, ldk, q + (bh * N + t0) * D, kChunk, valid, D, fm);
     const float* st = total + bh * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) S[e] = st[e];
     __syncthreads();
@@ -298,9 +298,10 @@ __device__ __forceinline__ int col_of(bool b_kmajor, int tc, int y) {
 }
 
 // acc[x][y] += sum_{k0 <= k < k1} Aop(4 tr + x, k) Bop(k, col_of(y)), k0 and k1
-// multiples of 4. Aop(r, k) is A[r kLd + k] (row-major) or A[k kLd + r]
-// (k-major); Bop(k, c) is B[k kLd + c] (k-major) or B[c kLd + k] (column-major).
-template <bool kAKmaj, bool kBKmaj>
+// multiples of 4. Aop(r, k) is A[r kLdA + k] (row-major) or A[k kLdA + r]
+// (k-major); Bop(k, c) is B[k kLdB + c] (k-major) or B[c kLdB + k] (column-major).
+// Row lengths other than 68 keep the bank pattern when they are 4 mod 32.
+template <bool kAKmaj, bool kBKmaj, int kLdA = kLd, int kLdB = kLd>
 __device__ __forceinline__ void mm4(float (&acc)[4][4], const float* A, const float* B, int k0,
                                     int k1, int tr, int tc) {
 #pragma unroll 2
@@ -309,17 +310,17 @@ __device__ __forceinline__ void mm4(float (&acc)[4][4], const float* A, const fl
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (kAKmaj) {
-                const float4 f = *reinterpret_cast<const float4*>(A + (kk + i) * kLd + 4 * tr);
+                const float4 f = *reinterpret_cast<const float4*>(A + (kk + i) * kLdA + 4 * tr);
                 a[0][i] = f.x, a[1][i] = f.y, a[2][i] = f.z, a[3][i] = f.w;
             } else {
-                const float4 f = *reinterpret_cast<const float4*>(A + (4 * tr + i) * kLd + kk);
+                const float4 f = *reinterpret_cast<const float4*>(A + (4 * tr + i) * kLdA + kk);
                 a[i][0] = f.x, a[i][1] = f.y, a[i][2] = f.z, a[i][3] = f.w;
             }
             if (kBKmaj) {
-                const float4 f = *reinterpret_cast<const float4*>(B + (kk + i) * kLd + 4 * tc);
+                const float4 f = *reinterpret_cast<const float4*>(B + (kk + i) * kLdB + 4 * tc);
                 b[i][0] = f.x, b[i][1] = f.y, b[i][2] = f.z, b[i][3] = f.w;
             } else {
-                const float4 f = *reinterpret_cast<const float4*>(B + (tc + 16 * i) * kLd + kk);
+                const float4 f = *reinterpret_cast<const float4*>(B + (tc + 16 * i) * kLdB + kk);
                 b[0][i] = f.x, b[1][i] = f.y, b[2][i] = f.z, b[3][i] = f.w;
             }
         }
@@ -339,13 +340,13 @@ __device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
         for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
 }
 
-// A [64][width] global tile into shared rows of kLd floats (phi applied when
-// `with_phi`); rows >= valid and columns >= width are zero. The trip count is
+// A [64][width] global tile into shared rows of kLd floats (feature map `fm`
+// applied unless kNoMap); rows >= valid and columns >= width are zero. The trip count is
 // fixed so that each thread's 16 loads are in flight together.
 constexpr int kPerThread = kChunk * kChunk / kThreads;
 template <typename T>
 __device__ __forceinline__ void load_tile(float* dst, const T* src, int valid, int width,
-                                          bool with_phi) {
+                                          int fm) {
     float x[kPerThread];
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
@@ -355,7 +356,7 @@ __device__ __forceinline__ void load_tile(float* dst, const T* src, int valid, i
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
         const int idx = threadIdx.x + u * kThreads, r = idx >> 6, c = idx & 63;
-        dst[r * kLd + c] = (with_phi && r < valid && c < width) ? phi(x[u]) : x[u];
+        dst[r * kLd + c] = (fm != kNoMap && r < valid && c < width) ? fmap(x[u], fm) : x[u];
     }
 }
 
@@ -400,7 +401,7 @@ template <typename T, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2) bwd_rows_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ dout, const float* __restrict__ states, float* __restrict__ rowg,
-    float* __restrict__ rstates, int N, int D, int M, float eps) {
+    float* __restrict__ rstates, int N, int D, int M, float eps, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd] each
     float* fK = fQ + kChunk * kLd;
@@ -418,12 +419,12 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_rows_kernel(
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
     const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
-    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, fm);
     if (kCausal) {
-        load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
-        load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+        load_tile(fK, k + (bh * N + t0) * D, valid, D, fm);
+        load_tile(sV, v + (bh * N + t0) * M, valid, M, kNoMap);
     }
-    load_tile(sG, dout + (bh * N + t0) * M, valid, M, false);
+    load_tile(sG, dout + (bh * N + t0) * M, valid, M, kNoMap);
     const float* st = states + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
     load_state(P, st, D, M, false);
     for (int idx = t; idx < kChunk; idx += blockDim.x) zP[idx] = idx < D ? st[D * M + idx] : 0.f;
@@ -543,7 +544,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) chunk_state_tiled_kernel(const T* __restrict__ k,
                                                              const T* __restrict__ v,
                                                              float* __restrict__ states, int N,
-                                                             int D, int M) {
+                                                             int D, int M, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fK = sm;                       // [64][kLd]
     float* sV = fK + kChunk * kLd;
@@ -552,8 +553,8 @@ __global__ void __launch_bounds__(kThreads) chunk_state_tiled_kernel(const T* __
     const int t0 = c * kChunk;
     const int valid = min(kChunk, N - t0);
     const int t = threadIdx.x, tr = t >> 4, tc = t & 15;
-    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
-    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, fm);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, kNoMap);
     __syncthreads();
     float* out = states + (bh * nchunks + c) * (int64_t)(D * M + D);
     float acc[4][4];
@@ -582,7 +583,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ states, const float* __restrict__ rstates,
     const float* __restrict__ rowg, T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv,
-    int N, int D, int M) {
+    int N, int D, int M, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd] each
     float* fK = fQ + kChunk * kLd;
@@ -601,9 +602,9 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
     const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5;
-    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
-    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
-    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, fm);
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, fm);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, kNoMap);
     const float* rg = rowg + (bh * N + t0) * (int64_t)(M + 1);
     const float* st = states + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
     const float* rs = rstates + (bh * nchunks + (kCausal ? c : 0)) * (int64_t)E;
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
             const int i = 4 * tr + x, d = col_of(true, tc, y);
             if (i < valid && d < D) {
                 const float s2 = fmaf(zP[d], dd[i], acc[x][y]);
-                dqc[(int64_t)i * D + d] = from_f<T>(s2 * fminf(fQ[i * kLd + d], 1.f));
+                dqc[(int64_t)i * D + d] = from_f<T>(s2 * fmap_grad(fQ[i * kLd + d], fm));
             }
         }
     if (kCausal) {
@@ -670,7 +671,8 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
         for (int y = 0; y < 4; ++y) {
             const int j = 4 * tr + x, d = col_of(true, tc, y);
             if (j < valid && d < D)
-                dkc[(int64_t)j * D + d] = from_f<T>((acc[x][y] + rr[d]) * fminf(fK[j * kLd + d], 1.f));
+                dkc[(int64_t)j * D + d] =
+                    from_f<T>((acc[x][y] + rr[d]) * fmap_grad(fK[j * kLd + d], fm));
         }
     if (kCausal) __syncthreads();
     // dv = phi(K) R_next + W^T dnum; rows j, columns m.
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) chunk_output_tiled_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    const float* __restrict__ states, T* __restrict__ o, int N, int D, int M, float eps) {
+    const float* __restrict__ states, T* __restrict__ o, int N, int D, int M, float eps, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd] each
     float* fK = fQ + kChunk * kLd;
@@ -710,9 +712,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_output_tiled_kernel(
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
     const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
-    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
-    load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
-    load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, fm);
+    load_tile(fK, k + (bh * N + t0) * D, valid, D, fm);
+    load_tile(sV, v + (bh * N + t0) * M, valid, M, kNoMap);
     const float* st = states + (bh * nchunks + c) * (int64_t)E;
     load_state(P, st, D, M, false);
     for (int idx = t; idx < kChunk; idx += blockDim.x) zP[idx] = idx < D ? st[D * M + idx] : 0.f;
@@ -751,8 +753,9 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_output_tiled_kernel(
 
 template <typename T>
 cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* o, int64_t BH,
-                             int N, int D, int M, float eps, const float* S0, const float* z0,
-                             float* S_out, float* z_out, float* states, cudaStream_t st) {
+                             int N, int D, int M, float eps, int fm, const float* S0,
+                             const float* z0, float* S_out, float* z_out, float* states,
+                             cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     dim3 grid(nchunks, (unsigned)BH);
     const bool tiled = D <= kChunk && M <= kChunk;
@@ -769,7 +772,7 @@ cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* 
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
             return err;
         chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states,
-                                                                 N, D, M);
+                                                                 N, D, M, fm);
     } else {
         if ((err = cudaFuncSetAttribute(chunk_state_kernel<T>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
@@ -777,17 +780,17 @@ cudaError_t simt_causal_impl(const void* q, const void* k, const void* v, void* 
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
             return err;
         chunk_state_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D,
-                                                           M);
+                                                           M, fm);
     }
     const int64_t total = BH * (int64_t)(D * M + D);
     chunk_scan_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, S0, z0, S_out,
                                                                         z_out, BH, nchunks, D, M);
     if (tiled)
         chunk_output_tiled_kernel<T><<<grid, kThreads, sm3, st>>>(
-            (const T*)q, (const T*)k, (const T*)v, states, (T*)o, N, D, M, eps);
+            (const T*)q, (const T*)k, (const T*)v, states, (T*)o, N, D, M, eps, fm);
     else
         chunk_output_kernel<T><<<grid, kThreads, sm3, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                                            states, (T*)o, N, D, M, eps);
+                                                            states, (T*)o, N, D, M, eps, fm);
     return cudaPeekAtLastError();
 }
 
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kThreads) nc_partial_tiled_kernel(const T* __r
                                                                     const T* __restrict__ v,
                                                                     float* __restrict__ partials,
                                                                     int N, int D, int M,
-                                                                    int tokens_per_split) {
+                                                                    int tokens_per_split, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fK = sm;                       // [64][kLd]
     float* sV = fK + kChunk * kLd;
@@ -814,8 +817,8 @@ __global__ void __launch_bounds__(kThreads) nc_partial_tiled_kernel(const T* __r
     for (int t0 = begin; t0 < end; t0 += kChunk) {
         const int valid = min(kChunk, end - t0);
         __syncthreads();
-        load_tile(fK, k + (bh * N + t0) * D, valid, D, true);
-        load_tile(sV, v + (bh * N + t0) * M, valid, M, false);
+        load_tile(fK, k + (bh * N + t0) * D, valid, D, fm);
+        load_tile(sV, v + (bh * N + t0) * M, valid, M, kNoMap);
         __syncthreads();
         mm4<true, true>(acc, fK, sV, 0, kChunk, tr, tc);
         if (t < D)
@@ -838,7 +841,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) nc_apply_tiled_kernel(const T* __restrict__ q,
                                                                   const float* __restrict__ total,
                                                                   T* __restrict__ o, int N, int D,
-                                                                  int M, float eps) {
+                                                                  int M, float eps, int fm) {
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd]
     float* S = fQ + kChunk * kLd;         // [d][m]
@@ -849,7 +852,7 @@ __global__ void __launch_bounds__(kThreads) nc_apply_tiled_kernel(const T* __res
     const int valid = min(kChunk, N - t0);
     const int E = D * M + D;
     const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
-    load_tile(fQ, q + (bh * N + t0) * D, valid, D, true);
+    load_tile(fQ, q + (bh * N + t0) * D, valid, D, fm);
     const float* st = total + bh * E;
     load_state(S, st, D, M, false);
     for (int idx = t; idx < kChunk; idx += blockDim.x) z[idx] = idx < D ? st[D * M + idx] : 0.f;
@@ -877,7 +880,7 @@ __global__ void __launch_bounds__(kThreads) nc_apply_tiled_kernel(const T* __res
 
 template <typename T>
 cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, void* o,
-                                int64_t BH, int N, int D, int M, float eps, int nsplit,
+                                int64_t BH, int N, int D, int M, float eps, int fm, int nsplit,
                                 float* partials, float* total, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     const int per_split = ((nchunks + nsplit - 1) / nsplit) * kChunk;
@@ -895,7 +898,7 @@ cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, voi
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
             return err;
         nc_partial_tiled_kernel<T><<<dim3(nsplit, (unsigned)BH), kThreads, sm1, st>>>(
-            (const T*)k, (const T*)v, partials, N, D, M, per_split);
+            (const T*)k, (const T*)v, partials, N, D, M, per_split, fm);
     } else {
         if ((err = cudaFuncSetAttribute(nc_partial_kernel<T>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
@@ -903,7 +906,7 @@ cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, voi
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
             return err;
         nc_partial_kernel<T><<<dim3(nsplit, (unsigned)BH), kThreads, sm1, st>>>(
-            (const T*)k, (const T*)v, partials, N, D, M, per_split);
+            (const T*)k, (const T*)v, partials, N, D, M, per_split, fm);
     }
     const int E = D * M + D;
     const int64_t tot = BH * (int64_t)E;
@@ -911,16 +914,75 @@ cudaError_t simt_noncausal_impl(const void* q, const void* k, const void* v, voi
                                                                      E);
     if (tiled)
         nc_apply_tiled_kernel<T><<<dim3(nchunks, (unsigned)BH), kThreads, sm3, st>>>(
-            (const T*)q, total, (T*)o, N, D, M, eps);
+            (const T*)q, total, (T*)o, N, D, M, eps, fm);
     else
         nc_apply_kernel<T><<<dim3(nchunks, (unsigned)BH), kThreads, sm3, st>>>(
-            (const T*)q, total, (T*)o, N, D, M, eps);
+            (const T*)q, total, (T*)o, N, D, M, eps, fm);
+    return cudaPeekAtLastError();
+}
+
+// grid (ceil(rows / 64), ceil(R / 64)): positive random features of 64 rows x
+// 64 features, out[i, r] = exp(w_r . x_i - |x_i|^2 / 2 - shift) * scale with
+// scale = 1 / sqrt(R); the projections register-tiled, D <= kLdX - 4.
+template <typename T, int kLdX>
+__global__ void __launch_bounds__(kThreads) random_features_kernel(
+    const T* __restrict__ x, const T* __restrict__ W, T* __restrict__ out, int64_t rows, int D,
+    int R, float shift, float scale) {
+    extern __shared__ __align__(16) float sm[];
+    float* X = sm;                        // [64][kLdX]: the block's rows of x
+    float* Wt = X + kChunk * kLdX;        // [64][kLdX]: the block's rows of W
+    float* hsq = Wt + kChunk * kLdX;      // [64]: |x_i|^2 / 2
+    const int64_t r0 = (int64_t)blockIdx.x * kChunk;
+    const int f0 = blockIdx.y * kChunk;
+    const int vrows = (int)min((int64_t)kChunk, rows - r0);
+    const int vfeat = min(kChunk, R - f0);
+    const int Dp = (D + 3) & ~3;          // the sums run to a multiple of 4 over zeros
+    const int t = threadIdx.x, tr = t >> 4, tc = t & 15, warp = t >> 5, lane = t & 31;
+#pragma unroll 4
+    for (int idx = t; idx < kChunk * Dp; idx += kThreads) {
+        const int r = idx / Dp, d = idx - r * Dp;
+        X[r * kLdX + d] = (r < vrows && d < D) ? to_f(x[(r0 + r) * D + d]) : 0.f;
+        Wt[r * kLdX + d] = (r < vfeat && d < D) ? to_f(W[(int64_t)(f0 + r) * D + d]) : 0.f;
+    }
+    __syncthreads();
+    for (int i = warp; i < kChunk; i += kThreads / 32) {
+        float s2 = 0.f;
+        for (int d = lane; d < Dp; d += 32) s2 = fmaf(X[i * kLdX + d], X[i * kLdX + d], s2);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        if (lane == 0) hsq[i] = 0.5f * s2;
+    }
+    __syncthreads();
+    float acc[4][4];
+    zero4x4(acc);
+    mm4<false, false, kLdX, kLdX>(acc, X, Wt, 0, Dp, tr, tc);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int i = 4 * tr + a, c = col_of(false, tc, y);
+            if (i < vrows && c < vfeat)
+                out[(r0 + i) * R + f0 + c] = from_f<T>(expf(acc[a][y] - hsq[i] - shift) * scale);
+        }
+}
+
+template <typename T, int kLdX>
+cudaError_t random_features_impl(const void* x, const void* W, void* out, int64_t rows, int D,
+                                 int R, float shift, cudaStream_t st) {
+    const size_t smem = sizeof(float) * (2 * (size_t)kChunk * kLdX + kChunk);
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(random_features_kernel<T, kLdX>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return err;
+    const dim3 grid((unsigned)((rows + kChunk - 1) / kChunk), (unsigned)((R + kChunk - 1) / kChunk));
+    random_features_kernel<T, kLdX><<<grid, kThreads, smem, st>>>(
+        (const T*)x, (const T*)W, (T*)out, rows, D, R, shift, 1.f / sqrtf((float)R));
     return cudaPeekAtLastError();
 }
 
 template <typename T, bool kCausal>
 cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const void* dout, void* dq,
-                          void* dk, void* dv, int64_t BH, int N, int D, int M, float eps,
+                          void* dk, void* dv, int64_t BH, int N, int D, int M, float eps, int fm,
                           float* states, float* rstates, float* rowg, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     dim3 grid(nchunks, (unsigned)BH);
@@ -938,21 +1000,23 @@ cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const voi
     const int E = D * M + D;
     const int64_t total = BH * (int64_t)E;
     const unsigned sgrid = (unsigned)((total + 255) / 256);
-    chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D, M);
+    chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D,
+                                                             M, fm);
     if (kCausal)
         chunk_scan_kernel<<<sgrid, 256, 0, st>>>(states, nullptr, nullptr, nullptr, nullptr, BH,
                                                  nchunks, D, M);
     else
         chunk_total_kernel<<<sgrid, 256, 0, st>>>(states, BH, nchunks, E);
     bwd_rows_kernel<T, kCausal><<<grid, kThreads, sm2, st>>>(
-        (const T*)q, (const T*)k, (const T*)v, (const T*)dout, states, rowg, rstates, N, D, M, eps);
+        (const T*)q, (const T*)k, (const T*)v, (const T*)dout, states, rowg, rstates, N, D, M, eps,
+        fm);
     if (kCausal)
         chunk_rscan_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
     else
         chunk_total_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
     bwd_grad_kernel<T, kCausal><<<grid, kThreads, sm3, st>>>(
         (const T*)q, (const T*)k, (const T*)v, states, rstates, rowg, (T*)dq, (T*)dk, (T*)dv, N, D,
-        M);
+        M, fm);
     return cudaPeekAtLastError();
 }
 
@@ -978,27 +1042,27 @@ size_t simt_noncausal_workspace(int64_t BH, int N, int D, int M) {
 }
 
 cudaError_t simt_causal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                        int64_t BH, int N, int D, int M, float eps, const float* S0,
+                        int64_t BH, int N, int D, int M, float eps, int fm, const float* S0,
                         const float* z0, float* S_out, float* z_out, void* scratch,
                         cudaStream_t st) {
     float* states = (float*)scratch;
     if (dt == LA_F32)
-        return simt_causal_impl<float>(q, k, v, o, BH, N, D, M, eps, S0, z0, S_out, z_out,
+        return simt_causal_impl<float>(q, k, v, o, BH, N, D, M, eps, fm, S0, z0, S_out, z_out,
                                        states, st);
-    return simt_causal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, S0, z0, S_out, z_out,
+    return simt_causal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, fm, S0, z0, S_out, z_out,
                                            states, st);
 }
 
 cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o, la_dtype dt,
-                           int64_t BH, int N, int D, int M, float eps, void* scratch,
+                           int64_t BH, int N, int D, int M, float eps, int fm, void* scratch,
                            cudaStream_t st) {
     const int nsplit = simt_noncausal_splits(BH, N);
     float* partials = (float*)scratch;
     float* total = partials + (size_t)BH * nsplit * (size_t)(D * M + D);
     if (dt == LA_F32)
-        return simt_noncausal_impl<float>(q, k, v, o, BH, N, D, M, eps, nsplit, partials, total,
-                                          st);
-    return simt_noncausal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, nsplit, partials,
+        return simt_noncausal_impl<float>(q, k, v, o, BH, N, D, M, eps, fm, nsplit, partials,
+                                          total, st);
+    return simt_noncausal_impl<__nv_bfloat16>(q, k, v, o, BH, N, D, M, eps, fm, nsplit, partials,
                                               total, st);
 }
 
@@ -1010,20 +1074,29 @@ size_t simt_bwd_workspace(int64_t BH, int N, int D, int M) {
 
 cudaError_t simt_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq,
                      void* dk, void* dv, la_dtype dt, bool causal, int64_t BH, int N, int D, int M,
-                     float eps, void* scratch, cudaStream_t st) {
+                     float eps, int fm, void* scratch, cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     float* states = (float*)scratch;
     float* rstates = states + (size_t)BH * nchunks * (size_t)(D * M + D);
     float* rowg = rstates + (size_t)BH * nchunks * (size_t)(D * M + D);
     if (dt == LA_F32)
-        return causal ? simt_bwd_impl<float, true>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+        return causal ? simt_bwd_impl<float, true>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, fm,
                                                    states, rstates, rowg, st)
-                      : simt_bwd_impl<float, false>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+                      : simt_bwd_impl<float, false>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps, fm,
                                                     states, rstates, rowg, st);
     return causal ? simt_bwd_impl<__nv_bfloat16, true>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
-                                                       states, rstates, rowg, st)
+                                                       fm, states, rstates, rowg, st)
                   : simt_bwd_impl<__nv_bfloat16, false>(q, k, v, dout, dq, dk, dv, BH, N, D, M,
-                                                        eps, states, rstates, rowg, st);
+                                                        eps, fm, states, rstates, rowg, st);
+}
+
+cudaError_t simt_random_features(const void* x, const void* W, void* out, la_dtype dt,
+                                 int64_t rows, int D, int R, float shift, cudaStream_t st) {
+    if (dt == LA_F32)
+        return D <= 64 ? random_features_impl<float, 68>(x, W, out, rows, D, R, shift, st)
+                       : random_features_impl<float, 132>(x, W, out, rows, D, R, shift, st);
+    return D <= 64 ? random_features_impl<__nv_bfloat16, 68>(x, W, out, rows, D, R, shift, st)
+                   : random_features_impl<__nv_bfloat16, 132>(x, W, out, rows, D, R, shift, st);
 }
 
 }  // namespace la

@@ -68,8 +68,12 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
     return r;
 }
 
+// The feature map on eight packed bf16 values: elu + 1, or (kPhiIdentity) the
+// values as they are, for features the caller has already computed.
+template <int kPhi = kPhiElu1>
 __device__ __forceinline__ uint4 phi8(uint4 u) {
-    return make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
+    if constexpr (kPhi == kPhiIdentity) return u;
+    else return make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
 }
 
 __device__ __forceinline__ void named_bar(int id, int threads) {
@@ -95,6 +99,7 @@ __device__ __forceinline__ void report_timeout(WsHeader* hdr) {
 
 // phi in place on the 128 x 64 bf16 tile rows (t >> 3) + 32 k, physical chunk
 // (t & 7), for a 256-thread group; rows >= zero_from are set to 0.
+template <int kPhi = kPhiElu1>
 __device__ __forceinline__ void phi_tile_256(uint8_t* tile, int t, int zero_from) {
     uint4 v[4];
 #pragma unroll
@@ -103,13 +108,14 @@ __device__ __forceinline__ void phi_tile_256(uint8_t* tile, int t, int zero_from
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int r = (t >> 3) + 32 * k;
-        const uint4 o = r < zero_from ? phi8(v[k]) : make_uint4(0, 0, 0, 0);
+        const uint4 o = r < zero_from ? phi8<kPhi>(v[k]) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(tile + r * 128 + (t & 7) * 16) = o;
     }
 }
 
 // phi_tile_256 on two tiles at once: all eight loads are issued before any
 // store, so the two tiles' shared-memory latencies overlap.
+template <int kPhi = kPhiElu1>
 __device__ __forceinline__ void phi_tiles2_256(uint8_t* ta, int zero_a, uint8_t* tb, int zero_b,
                                                int t) {
     uint4 v[8];
@@ -120,7 +126,7 @@ __device__ __forceinline__ void phi_tiles2_256(uint8_t* ta, int zero_a, uint8_t*
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int r = (t >> 3) + 32 * (k & 3);
-        const uint4 o = r < (k < 4 ? zero_a : zero_b) ? phi8(v[k]) : make_uint4(0, 0, 0, 0);
+        const uint4 o = r < (k < 4 ? zero_a : zero_b) ? phi8<kPhi>(v[k]) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>((k < 4 ? ta : tb) + r * 128 + (t & 7) * 16) = o;
     }
 }

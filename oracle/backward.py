@@ -25,9 +25,13 @@ import numpy as np
 import torch
 
 
-def _phi(x):
+def _phi(x, phi="elu1"):
     # elu(x) + 1: x + 1 for x > 0, e^x for x <= 0 (the exp branch is evaluated
-    # on min(x, 0) so that its unused values never overflow).
+    # on min(x, 0) so that its unused values never overflow). "identity": the
+    # inputs are already features (the method leaves phi free, "Why Replace
+    # Attention?", section 4.5).
+    if phi == "identity":
+        return x
     return torch.where(x > 0, x + 1.0, torch.exp(torch.clamp(x, max=0.0)))
 
 
@@ -35,16 +39,16 @@ def _t(a):
     return torch.tensor(np.asarray(a, dtype=np.float64), dtype=torch.float64)
 
 
-def forward_quadratic(q, k, v, causal, eps=1e-6):
-    fq, fk = _phi(q), _phi(k)
+def forward_quadratic(q, k, v, causal, eps=1e-6, phi="elu1"):
+    fq, fk = _phi(q, phi), _phi(k, phi)
     w = fq @ fk.transpose(-1, -2)
     if causal:
         w = torch.tril(w)
     return (w @ v) / (w.sum(-1, keepdim=True) + eps)
 
 
-def forward_recurrent(q, k, v, causal, eps=1e-6):
-    fq, fk = _phi(q), _phi(k)
+def forward_recurrent(q, k, v, causal, eps=1e-6, phi="elu1"):
+    fq, fk = _phi(q, phi), _phi(k, phi)
     N = q.shape[-2]
     S = torch.zeros(q.shape[:-2] + (q.shape[-1], v.shape[-1]), dtype=q.dtype)
     z = torch.zeros(q.shape[:-2] + (q.shape[-1],), dtype=q.dtype)
@@ -61,21 +65,22 @@ def forward_recurrent(q, k, v, causal, eps=1e-6):
     return torch.stack(rows, dim=-2)
 
 
-def grads(q, k, v, dout, causal=True, eps=1e-6, form="quadratic"):
+def grads(q, k, v, dout, causal=True, eps=1e-6, form="quadratic", phi="elu1"):
     """dL/dq, dL/dk, dL/dv for L = sum(o * dout); inputs [..., N, D] / [..., N, M].
 
     Returns float64 numpy arrays. `form` selects the forward definition the
-    derivative is taken of ("quadratic" or "recurrent")."""
+    derivative is taken of ("quadratic" or "recurrent"); `phi` the feature map
+    ("elu1" or "identity")."""
     qt, kt, vt = (_t(a).requires_grad_(True) for a in (q, k, v))
     g = _t(dout)
     fwd = forward_quadratic if form == "quadratic" else forward_recurrent
-    o = fwd(qt, kt, vt, causal, eps)
+    o = fwd(qt, kt, vt, causal, eps, phi)
     (o * g).sum().backward()
     return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
 
 
-def forward(q, k, v, causal=True, eps=1e-6, form="quadratic"):
+def forward(q, k, v, causal=True, eps=1e-6, form="quadratic", phi="elu1"):
     """The forward of the chosen form, as a float64 numpy array."""
     fwd = forward_quadratic if form == "quadratic" else forward_recurrent
     with torch.no_grad():
-        return fwd(_t(q), _t(k), _t(v), causal, eps).numpy()
+        return fwd(_t(q), _t(k), _t(v), causal, eps, phi).numpy()

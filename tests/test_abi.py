@@ -56,6 +56,23 @@ def test_workspace_size(lib):
         assert lib.la_workspace_size(op, 8, 8, 0, 64, 64, lib.LA_BF16) == 256
 
 
+def test_feature_map_entries_reject_bad_arguments_without_a_gpu(lib):
+    so = ctypes.CDLL(lib.library_path())
+    P = ctypes.c_void_p
+    so.la_noncausal_fwd_phi.argtypes = [P, P, P, P] + [ctypes.c_int] * 7 + [ctypes.c_float, P,
+                                                                            ctypes.c_size_t, P]
+    # An unknown feature map is refused before anything is launched.
+    assert so.la_noncausal_fwd_phi(None, None, None, None, 1, 1, 0, 64, 64, 1, 5, 1e-6, None, 0,
+                                   None) == 1
+    so.la_positive_random_features.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_float, P]
+    assert so.la_positive_random_features(None, None, None, 10, 129, 64, 1, 0.0, None) == 1
+    assert so.la_positive_random_features(None, None, None, 10, 64, 0, 1, 0.0, None) == 1
+    assert so.la_positive_random_features(None, None, None, 10, 64, 64, 1, float("inf"), None) == 1
+    assert so.la_positive_random_features(None, None, None, 10, 64, 64, 1, 0.0, None) == 1  # null x
+    assert so.la_positive_random_features(None, None, None, 0, 64, 64, 1, 0.0, None) == 0   # empty
+
+
 def test_backward_workspace_and_launches(lib):
     # Both backward directions use the same scratch: per-chunk forward and reverse
     # sums (B*H*ceil(N/64)*(Dk*Dv + Dk) floats each) and per-row (dnum, dden)

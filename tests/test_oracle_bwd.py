@@ -18,6 +18,17 @@ def _rand(rng, *shape):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+def test_identity_map_matches_the_feature_oracle(causal):
+    # The identity-map forward on features equals the numpy feature-map oracle,
+    # itself pinned against the C oracle on elu + 1 features.
+    from oracle import feature_maps as fm
+    rng = np.random.default_rng(5)
+    fq, fk, v = rng.random((2, 23, 4)), rng.random((2, 23, 4)), _rand(rng, 2, 23, 3)
+    np.testing.assert_allclose(bwd.forward(fq, fk, v, causal, phi="identity"),
+                               fm.attention_from_features(fq, fk, v, causal), rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_forward_matches_c_oracle(causal):
     rng = np.random.default_rng(0)
     q, k, v = _rand(rng, 2, 37, 5), _rand(rng, 2, 37, 5), _rand(rng, 2, 37, 3)
@@ -26,13 +37,16 @@ def test_forward_matches_c_oracle(causal):
     np.testing.assert_allclose(bwd.forward(q, k, v, causal, form="recurrent"), ref, rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("causal", [True, False])
-def test_gradients_match_central_differences(causal):
+@pytest.mark.parametrize("causal,phi", [(True, "elu1"), (False, "elu1"), (True, "identity"),
+                                        (False, "identity")])
+def test_gradients_match_central_differences(causal, phi):
     rng = np.random.default_rng(1)
     N, D, M = 6, 3, 2
     q, k, v, g = _rand(rng, N, D), _rand(rng, N, D), _rand(rng, N, M), _rand(rng, N, M)
-    dq, dk, dv = bwd.grads(q, k, v, g, causal)
-    loss = lambda q_, k_, v_: float((bwd.forward(q_, k_, v_, causal) * g).sum())
+    if phi == "identity":       # non-negative features keep the denominators away from 0
+        q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+    dq, dk, dv = bwd.grads(q, k, v, g, causal, phi=phi)
+    loss = lambda q_, k_, v_: float((bwd.forward(q_, k_, v_, causal, phi=phi) * g).sum())
     h = 1e-6
     for name, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
         fd = np.zeros_like(x)

@@ -65,6 +65,19 @@ def make_qkv(B, H, N, D, dtype="f32", seed=0, k_scale=1.0, Dv=None):
     return q.to(dt), k.to(dt), v.to(dt)
 
 
+def make_features(B, H, N, C, dtype="f32", seed=0, Dv=None):
+    """Non-negative feature inputs fq, fk [B,H,N,C] (uniform on [0, 1)) and v [B,H,N,Dv]
+    (standard normal) as CPU tensors, for the identity feature map."""
+    Dv = C if Dv is None else Dv
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    fq = torch.rand((B, H, N, C), generator=g, dtype=torch.float32)
+    fk = torch.rand((B, H, N, C), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, N, Dv), generator=g, dtype=torch.float32)
+    dt = torch_dtype(dtype)
+    return fq.to(dt), fk.to(dt), v.to(dt)
+
+
 def make_workload(w: Workload, seed=0):
     return make_qkv(w.B, w.H, w.N, w.D, w.dtype, seed=seed, k_scale=w.k_scale)
 
