@@ -385,6 +385,49 @@ def other_paths(la, dev, stream):
                     "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
                     "bound": "alu (fp32 FMA)"}
         del ws, g
+    # Positive random features (R = 64, x scaled by D^-1/4) of q and k, then the
+    # identity-map causal forward on the tensor-core path, at the image shape.
+    R = 64
+    W = torch.randn(R, w.D, device=dev, generator=gen).bfloat16()
+    qs, ks = (q.float() * w.D ** -0.25).bfloat16(), (k.float() * w.D ** -0.25).bfloat16()
+    fq = torch.empty(w.B, w.H, w.N, R, device=dev, dtype=torch.bfloat16)
+    fk = torch.empty_like(fq)
+    o = torch.empty_like(v)
+    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, R, w.D, q.dtype, dev)
+
+    def features():
+        la.la_positive_random_features(qs, W, out=fq)
+        la.la_positive_random_features(ks, W, out=fk)
+
+    def chain():
+        features()
+        la.la_causal_fwd(fq, fk, v, o=o, ws=ws, phi=la.LA_PHI_IDENTITY)
+
+    res = {}
+    for name, fn in (("features_ms", features), ("chain_ms", chain)):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / reps
+        del g
+    rows = 2 * w.tokens
+    flops = rows * 2 * R * w.D
+    out["random_features_causal"] = {
+        "workload": w.name.replace("causal", "random features (R=64) + identity-map causal"),
+        "value": w.tokens / (res["chain_ms"] * 1e-3), "unit": "tokens/s", **res,
+        "features_tflops": flops / (res["features_ms"] * 1e-3) / 1e12,
+        "features_frac_of_fp32_fma": flops / (res["features_ms"] * 1e-3) / FP32_FMA_PEAK,
+        "bound": "features: alu (fp32 FMA); attention: as the causal path"}
     return out
 
 

@@ -397,11 +397,12 @@ __device__ __forceinline__ void load_dnum(float* dst, const float* rg, int valid
 // the chunk's slot of `states` holds its carried-in state and the rows add the
 // masked in-chunk part; non-causal: chunk 0's slot holds the whole sequence's
 // (S, z), which every row sees.
-template <typename T, bool kCausal>
+template <typename T, bool kCausal, int kFm>
 __global__ void __launch_bounds__(kThreads, 2) bwd_rows_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ dout, const float* __restrict__ states, float* __restrict__ rowg,
-    float* __restrict__ rstates, int N, int D, int M, float eps, int fm) {
+    float* __restrict__ rstates, int N, int D, int M, float eps) {
+    constexpr int fm = kFm;
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd] each
     float* fK = fQ + kChunk * kLd;
@@ -578,12 +579,13 @@ __global__ void __launch_bounds__(kThreads) chunk_state_tiled_kernel(const T* __
 // (S_prev, z_prev), the carried-in reverse sums (R_next, r_next) and the rows'
 // dnum, dden. Non-causal: chunk 0's slots hold the whole sequence's (S, z) and
 // (R, r), and there are no in-chunk terms.
-template <typename T, bool kCausal>
+template <typename T, bool kCausal, int kFm>
 __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ states, const float* __restrict__ rstates,
     const float* __restrict__ rowg, T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv,
-    int N, int D, int M, int fm) {
+    int N, int D, int M) {
+    constexpr int fm = kFm;
     extern __shared__ __align__(16) float sm[];
     float* fQ = sm;                       // [64][kLd] each
     float* fK = fQ + kChunk * kLd;
@@ -980,10 +982,11 @@ cudaError_t random_features_impl(const void* x, const void* W, void* out, int64_
     return cudaPeekAtLastError();
 }
 
-template <typename T, bool kCausal>
-cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const void* dout, void* dq,
-                          void* dk, void* dv, int64_t BH, int N, int D, int M, float eps, int fm,
-                          float* states, float* rstates, float* rowg, cudaStream_t st) {
+template <typename T, bool kCausal, int kFm>
+cudaError_t simt_bwd_launch(const void* q, const void* k, const void* v, const void* dout,
+                            void* dq, void* dk, void* dv, int64_t BH, int N, int D, int M,
+                            float eps, float* states, float* rstates, float* rowg,
+                            cudaStream_t st) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     dim3 grid(nchunks, (unsigned)BH);
     const size_t sm1 = sizeof(float) * (2 * (size_t)kChunk * kLd);
@@ -992,32 +995,44 @@ cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const voi
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(chunk_state_tiled_kernel<T>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) ||
-        (err = cudaFuncSetAttribute(bwd_rows_kernel<T, kCausal>,
+        (err = cudaFuncSetAttribute(bwd_rows_kernel<T, kCausal, kFm>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) ||
-        (err = cudaFuncSetAttribute(bwd_grad_kernel<T, kCausal>,
+        (err = cudaFuncSetAttribute(bwd_grad_kernel<T, kCausal, kFm>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
         return err;
     const int E = D * M + D;
     const int64_t total = BH * (int64_t)E;
     const unsigned sgrid = (unsigned)((total + 255) / 256);
     chunk_state_tiled_kernel<T><<<grid, kThreads, sm1, st>>>((const T*)k, (const T*)v, states, N, D,
-                                                             M, fm);
+                                                             M, kFm);
     if (kCausal)
         chunk_scan_kernel<<<sgrid, 256, 0, st>>>(states, nullptr, nullptr, nullptr, nullptr, BH,
                                                  nchunks, D, M);
     else
         chunk_total_kernel<<<sgrid, 256, 0, st>>>(states, BH, nchunks, E);
-    bwd_rows_kernel<T, kCausal><<<grid, kThreads, sm2, st>>>(
-        (const T*)q, (const T*)k, (const T*)v, (const T*)dout, states, rowg, rstates, N, D, M, eps,
-        fm);
+    bwd_rows_kernel<T, kCausal, kFm><<<grid, kThreads, sm2, st>>>(
+        (const T*)q, (const T*)k, (const T*)v, (const T*)dout, states, rowg, rstates, N, D, M, eps);
     if (kCausal)
         chunk_rscan_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
     else
         chunk_total_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
-    bwd_grad_kernel<T, kCausal><<<grid, kThreads, sm3, st>>>(
+    bwd_grad_kernel<T, kCausal, kFm><<<grid, kThreads, sm3, st>>>(
         (const T*)q, (const T*)k, (const T*)v, states, rstates, rowg, (T*)dq, (T*)dk, (T*)dv, N, D,
-        M, fm);
+        M);
     return cudaPeekAtLastError();
+}
+
+// The feature map is a compile-time parameter of the backward kernels: taken at
+// run time it cost the gradient pass about 20 %.
+template <typename T, bool kCausal>
+cudaError_t simt_bwd_impl(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                          void* dk, void* dv, int64_t BH, int N, int D, int M, float eps, int fm,
+                          float* states, float* rstates, float* rowg, cudaStream_t st) {
+    if (fm == kPhiIdentity)
+        return simt_bwd_launch<T, kCausal, kPhiIdentity>(q, k, v, dout, dq, dk, dv, BH, N, D, M,
+                                                         eps, states, rstates, rowg, st);
+    return simt_bwd_launch<T, kCausal, kPhiElu1>(q, k, v, dout, dq, dk, dv, BH, N, D, M, eps,
+                                                 states, rstates, rowg, st);
 }
 
 }  // namespace
