@@ -322,6 +322,42 @@ def other_paths(la, dev, stream):
                      "frac_of_hbm": per_step / (us * 1e-6) / 1e9 / hbm,
                      "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
     del q, k, v, o, S, z, g
+    # Layer decode step at the same batch (512 sequences, d_model = 8 x 64, bf16,
+    # synthetic weights): QKV projection, the decode step, output projection.
+    dm = w.H * w.D
+    Wqkv = (torch.randn(dm, 3 * dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
+    Wo = (torch.randn(dm, dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
+    xs = torch.randn(T, w.B, dm, device=dev, generator=gen).bfloat16()
+    ys = torch.empty_like(xs)
+    S = torch.zeros(w.B, w.H, w.D, w.D, device=dev)
+    z = torch.zeros(w.B, w.H, w.D, device=dev)
+    ws = la.workspace(la.LA_OP_LAYER_DECODE, w.B, w.H, 1, w.D, w.D, xs.dtype, dev)
+
+    def layer_steps():
+        for t in range(T):
+            la.la_layer_decode_step(xs[t], Wqkv, Wo, S, z, w.H, y=ys[t], ws=ws)
+
+    layer_steps()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer_steps()
+    g.replay()
+    torch.cuda.synchronize()
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    lus = a.elapsed_time(b) / T * 1e3
+    gemm_flops = 2 * w.B * dm * 4 * dm
+    out["layer_decode"] = {
+        "workload": f"layer decode step, {w.B} sequences, d_model {dm} = {w.H} x {w.D}, bf16, "
+                    f"synthetic weights, {T} steps timed",
+        "value": 1e6 / lus, "unit": "steps/s", "us_per_step": lus,
+        "attention_share_est": us / lus,
+        "projection_tflops_if_rest": gemm_flops / max(lus - us, 1e-3) / 1e6,
+        "note": "projections are cuBLASLt bf16 GEMMs; the decode step between them is ours"}
+    del Wqkv, Wo, xs, ys, S, z, ws, g
     # Causal and non-causal forward on fp32 inputs (the fp32 SIMT path) at the
     # image shape B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
     w = WORKLOADS["image"]

@@ -71,7 +71,8 @@ typedef enum {
     LA_OP_CAUSAL = 1,
     LA_OP_DECODE = 2,
     LA_OP_CAUSAL_BWD = 3,
-    LA_OP_NONCAUSAL_BWD = 4
+    LA_OP_NONCAUSAL_BWD = 4,
+    LA_OP_LAYER_DECODE = 5
 } la_op;
 
 /*
@@ -310,6 +311,29 @@ la_status la_noncausal_bwd_phi(const void* q, const void* k, const void* v, cons
 la_status la_positive_random_features(const void* x, const void* W, void* out, int64_t rows,
                                       int D, int R, la_dtype dt, float shift,
                                       la_stream_t stream);
+
+/*
+ * One decode step of a linear-attention layer for B sequences (d_model = H D):
+ * [q | k | v] = x Wqkv; per head h the recurrent step S <- S + phi(k_h) v_h^T,
+ * z <- z + phi(k_h), o_h = phi(q_h)^T S / (phi(q_h)^T z + eps) (elu + 1);
+ * y = [o_1 | ... | o_H] Wo ("Why Replace Attention? The Softmax Bottleneck and
+ * the Path to Linear Time", section 7.2, steps 1-4: k and v computed from the
+ * token's hidden state, then the update and the read).
+ *  - x: [B, d_model]; Wqkv: [d_model, 3 H D] (columns h D .. h D + D - 1 are
+ *    head h of q, then of k, then of v); Wo: [H D, d_model]; y: [B, d_model];
+ *    all row-major, dtype dt, device pointers, 16-byte aligned.
+ *  - S: [B, H, D, D], z: [B, H, D] float32, read and written in place.
+ *  - workspace: la_workspace_size(LA_OP_LAYER_DECODE, B, H, 1, D, D, dt, ...)
+ *    bytes (the projection buffers and cuBLASLt scratch), 256-byte aligned.
+ *  - The projections are cuBLASLt GEMMs with fp32 accumulation (the library's
+ *    one dependency beyond the CUDA runtime); the step between them is this
+ *    library's decode kernel, reading q, k, v in place in the projection. The
+ *    three launches go to `stream`; la_launch_count counts the library's own
+ *    kernel (1).
+ */
+la_status la_layer_decode_step(const void* x, const void* Wqkv, const void* Wo, void* y,
+                               float* S, float* z, int B, int H, int D, la_dtype dt, float eps,
+                               void* workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the workspace status word.

@@ -22,11 +22,13 @@ __all__ = [
     "la_noncausal_fwd", "la_causal_fwd", "la_decode_step", "la_query_status", "workspace",
     "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
     "la_causal_bwd", "LA_OP_CAUSAL_BWD", "la_noncausal_bwd", "LA_OP_NONCAUSAL_BWD",
-    "LA_PHI_ELU1", "LA_PHI_IDENTITY", "la_positive_random_features", "library_path",
+    "LA_PHI_ELU1", "LA_PHI_IDENTITY", "la_positive_random_features", "LA_OP_LAYER_DECODE",
+    "la_layer_decode_step", "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
 LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_BWD = 0, 1, 2, 3, 4
+LA_OP_LAYER_DECODE = 5
 LA_PHI_ELU1, LA_PHI_IDENTITY = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 
@@ -90,6 +92,8 @@ def _load():
     lib.la_noncausal_bwd_phi.restype = I
     lib.la_positive_random_features.argtypes = [P, P, P, L, I, I, I, F, P]
     lib.la_positive_random_features.restype = I
+    lib.la_layer_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
+    lib.la_layer_decode_step.restype = I
     lib.la_query_status.argtypes = [P, P]
     lib.la_query_status.restype = I
     return lib
@@ -376,6 +380,34 @@ def la_positive_random_features(x, W, out=None, shift=0.0, stream=None):
                                             float(shift), _stream(stream)),
            "la_positive_random_features")
     return out
+
+
+def la_layer_decode_step(x, Wqkv, Wo, S, z, H, y=None, eps=1e-6, ws=None, stream=None):
+    """One decode step of a linear-attention layer: x [B, d_model] -> y [B, d_model].
+
+    Wqkv [d_model, 3 H D] (q | k | v, head-major within each), Wo [H D, d_model];
+    S [B, H, D, D] and z [B, H, D] (float32) are updated in place."""
+    if x.dim() != 2 or Wqkv.dim() != 2 or Wo.dim() != 2:
+        raise ValueError("expected x [B, d_model], Wqkv [d_model, 3 H D], Wo [H D, d_model]")
+    B, dm = x.shape
+    D = dm // H if H else 0
+    if H * D != dm or tuple(Wqkv.shape) != (dm, 3 * dm) or tuple(Wo.shape) != (dm, dm):
+        raise ValueError("d_model must equal H D, Wqkv be [d_model, 3 d_model], Wo [d_model, d_model]")
+    if Wqkv.dtype != x.dtype or Wo.dtype != x.dtype:
+        raise TypeError("x, Wqkv and Wo must share one dtype")
+    if S.dtype != torch.float32 or z.dtype != torch.float32 or tuple(S.shape) != (B, H, D, D) \
+            or tuple(z.shape) != (B, H, D):
+        raise ValueError("S must be float32 [B,H,D,D] and z float32 [B,H,D]")
+    if y is None:
+        y = torch.empty_like(x)
+    _need_cuda(x, Wqkv, Wo, y, S, z, ws)
+    if ws is None:
+        ws = workspace(LA_OP_LAYER_DECODE, B, H, 1, D, D, x.dtype, x.device, stream)
+    _check(_lib.la_layer_decode_step(_ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(y), _ptr(S), _ptr(z), B,
+                                     H, D, _dt(x), float(eps), _ptr(ws), ws.numel(),
+                                     _stream(stream)),
+           "la_layer_decode_step")
+    return y
 
 
 def la_query_status(ws, stream=None):

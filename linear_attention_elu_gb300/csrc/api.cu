@@ -50,6 +50,8 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
         case LA_OP_CAUSAL_BWD:
         case LA_OP_NONCAUSAL_BWD:
             return la::simt_bwd_workspace(BH, N, Dk, Dv);
+        case LA_OP_LAYER_DECODE:
+            return la::layer_workspace(B, H, Dk, dt);
         default:
             return 0;
     }
@@ -147,10 +149,16 @@ la_status la_workspace_size(la_op op, int B, int H, int N, int Dk, int Dv, la_dt
                             size_t* bytes) {
     if (!bytes) return LA_ERR_INVALID_ARG;
     if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
-        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD)
+        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD && op != LA_OP_LAYER_DECODE)
         return LA_ERR_INVALID_ARG;
-    la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
+    const bool one_token = op == LA_OP_DECODE || op == LA_OP_LAYER_DECODE;
+    la_status s = check_common(B, H, one_token ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
+    if (op == LA_OP_LAYER_DECODE) {
+        if (Dk != Dv) return LA_ERR_UNSUPPORTED;
+        *bytes = kHeaderBytes + round_up(body_bytes(op, B, H, 1, Dk, Dv, dt), 256);
+        return LA_OK;
+    }
     if (op == LA_OP_DECODE) {
         *bytes = 0;
         return LA_OK;
@@ -166,16 +174,17 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
                           int* launches) {
     if (!launches) return LA_ERR_INVALID_ARG;
     if (op != LA_OP_CAUSAL && op != LA_OP_NONCAUSAL && op != LA_OP_DECODE &&
-        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD)
+        op != LA_OP_CAUSAL_BWD && op != LA_OP_NONCAUSAL_BWD && op != LA_OP_LAYER_DECODE)
         return LA_ERR_INVALID_ARG;
-    la_status s = check_common(B, H, op == LA_OP_DECODE ? 1 : N, Dk, Dv, dt);
+    const bool one_token = op == LA_OP_DECODE || op == LA_OP_LAYER_DECODE;
+    la_status s = check_common(B, H, one_token ? 1 : N, Dk, Dv, dt);
     if (s != LA_OK) return s;
     const int64_t BH = (int64_t)B * H;
-    if (BH == 0 || (op != LA_OP_DECODE && N == 0)) {
+    if (BH == 0 || (!one_token && N == 0)) {
         *launches = 0;
         return LA_OK;
     }
-    if (op == LA_OP_DECODE)
+    if (one_token)
         *launches = 1;
     else if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD)
         *launches = 5;

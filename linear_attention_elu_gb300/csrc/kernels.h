@@ -55,5 +55,13 @@ cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, i
 cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,
                         la_dtype dt, int64_t BH, int D, int M, float eps, int fm,
                         cudaStream_t st);
+// The same step with q, k of head h = b H + j at b ld_qk + j D and v at
+// b ld_v + j M (o stays contiguous [BH, M]).
+cudaError_t decode_step_strided(const void* q, const void* k, const void* v, void* o, float* S,
+                                float* z, la_dtype dt, int64_t BH, int D, int M, float eps, int fm,
+                                int H, int64_t ld_qk, int64_t ld_v, cudaStream_t st);
+
+// Layer decode step (csrc/layer.cu): workspace bytes after the header.
+size_t layer_workspace(int B, int H, int D, la_dtype dt);
 
 }  // namespace la

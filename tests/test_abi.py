@@ -160,3 +160,16 @@ def test_host_entry_rejects_bad_arguments_without_a_gpu(lib):
                                   p, 4096, p, 4096, None) == 1
     assert raw.la_causal_fwd_host(p, p, p, p, 1, 1, 8, 64, 64, 1, 1e-6, None, None,
                                   None, 0, p, 4096, None) == 3
+
+
+def test_layer_decode_workspace(lib):
+    # Projection buffers ([B, 3 d_model] and [B, d_model] in the dtype, each
+    # rounded up to 256 bytes) and 4 MiB of cuBLASLt scratch, after the header.
+    B, H, D = 512, 8, 64
+    dm = H * D
+    body = B * 3 * dm * 2 + B * dm * 2 + (4 << 20)
+    assert lib.la_workspace_size(lib.LA_OP_LAYER_DECODE, B, H, 1, D, D, lib.LA_BF16) == 256 + body
+    assert lib.la_launch_count(lib.LA_OP_LAYER_DECODE, B, H, 1, D, D, lib.LA_BF16) == 1
+    so = ctypes.CDLL(lib.library_path())
+    n = ctypes.c_size_t(0)
+    assert so.la_workspace_size(lib.LA_OP_LAYER_DECODE, B, H, 1, 64, 32, 1, ctypes.byref(n)) == 2
