@@ -362,6 +362,8 @@ la_status la_positive_random_features(const void* x, const void* W, void* out, i
     if ((s = check_tensor(x, rows * D, dt)) || (s = check_tensor(W, (int64_t)R * D, dt)) ||
         (s = check_tensor(out, rows * R, dt)))
         return s;
+    if (la::tc_random_features_supported(D, R, dt))
+        return from_cuda(la::tc_random_features(x, W, out, rows, shift, (cudaStream_t)stream));
     return from_cuda(la::simt_random_features(x, W, out, dt, rows, D, R, shift,
                                               (cudaStream_t)stream));
 }

@@ -37,6 +37,11 @@ cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o,
 cudaError_t simt_random_features(const void* x, const void* W, void* out, la_dtype dt,
                                  int64_t rows, int D, int R, float shift, cudaStream_t st);
 
+// Positive random features on the tensor cores: bf16, D = R = 64.
+bool tc_random_features_supported(int D, int R, la_dtype dt);
+cudaError_t tc_random_features(const void* x, const void* W, void* out, int64_t rows, float shift,
+                               cudaStream_t st);
+
 // Tensor-core (tcgen05) causal path: bf16, Dk = Dv = 64.
 bool tc_causal_supported(int D, int M, la_dtype dt);
 size_t tc_causal_workspace(int64_t BH, int N);

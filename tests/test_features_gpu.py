@@ -123,6 +123,9 @@ def test_backward_identity_map(la, causal, dt):
 
 
 @pytest.mark.parametrize("rows,D,R,dt", [
+    (1000, 64, 64, "bf16"),         # tensor-core path, ragged last tile
+    (100_000, 64, 64, "bf16"),      # tensor-core path, several tiles per CTA
+    (5, 64, 64, "bf16"),            # tensor-core path, one partial tile
     (1000, 64, 64, "f32"),
     (777, 64, 96, "bf16"),          # R not a multiple of 64
     (130, 128, 64, "f32"),          # the wide-row tile
