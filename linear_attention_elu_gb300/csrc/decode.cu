@@ -35,7 +35,7 @@ __device__ __forceinline__ HeadRow head_row(int64_t h, int H) {
 // feature map is a template parameter: selected at run time it cost the step
 // about 6 %.
 template <typename T, int kFm>
-__global__ void __launch_bounds__(256) decode64_kernel(const T* __restrict__ q,
+__global__ void __launch_bounds__(256, 4) decode64_kernel(const T* __restrict__ q,
                                                        const T* __restrict__ k,
                                                        const T* __restrict__ v,
                                                        T* __restrict__ o, float* __restrict__ S,
@@ -64,23 +64,30 @@ __global__ void __launch_bounds__(256) decode64_kernel(const T* __restrict__ q,
                                   to_f(vh[4 * g + 3]));
     float4* Sh = reinterpret_cast<float4*>(S + h * 64 * 64);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int r = 0; r < 32; ++r) {
-        const int row = 2 * r + par;
-        // Feature `row` lives in lane row & 31, register (row >> 5).
-        const float fkr = __shfl_sync(0xffffffffu, row < 32 ? fk0 : fk1, row & 31);
-        const float fqr = __shfl_sync(0xffffffffu, row < 32 ? fq0 : fq1, row & 31);
-        float4* p = Sh + row * 16 + g;
-        float4 s = *p;
-        s.x = fmaf(fkr, vv.x, s.x);
-        s.y = fmaf(fkr, vv.y, s.y);
-        s.z = fmaf(fkr, vv.z, s.z);
-        s.w = fmaf(fkr, vv.w, s.w);
-        *p = s;
-        acc.x = fmaf(fqr, s.x, acc.x);
-        acc.y = fmaf(fqr, s.y, acc.y);
-        acc.z = fmaf(fqr, s.z, acc.z);
-        acc.w = fmaf(fqr, s.w, acc.w);
+    // Rows in batches of 8: the batch's loads are all issued before any of its
+    // stores, so each lane keeps 8 state loads in flight.
+#pragma unroll
+    for (int r0 = 0; r0 < 32; r0 += 8) {
+        float4 sv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sv[u] = Sh[(2 * (r0 + u) + par) * 16 + g];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int row = 2 * (r0 + u) + par;
+            // Feature `row` lives in lane row & 31, register (row >> 5).
+            const float fkr = __shfl_sync(0xffffffffu, row < 32 ? fk0 : fk1, row & 31);
+            const float fqr = __shfl_sync(0xffffffffu, row < 32 ? fq0 : fq1, row & 31);
+            float4 s = sv[u];
+            s.x = fmaf(fkr, vv.x, s.x);
+            s.y = fmaf(fkr, vv.y, s.y);
+            s.z = fmaf(fkr, vv.z, s.z);
+            s.w = fmaf(fkr, vv.w, s.w);
+            Sh[row * 16 + g] = s;
+            acc.x = fmaf(fqr, s.x, acc.x);
+            acc.y = fmaf(fqr, s.y, acc.y);
+            acc.z = fmaf(fqr, s.z, acc.z);
+            acc.w = fmaf(fqr, s.w, acc.w);
+        }
     }
     // Rows were split by parity across the two half-warps: add the halves.
     acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 16);
