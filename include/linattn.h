@@ -231,7 +231,9 @@ la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, voi
 /*
  * Causal forward on HOST buffers: q, k, v, o are host pointers in the layout of
  * la_causal_fwd ([B,H,N,D], dtype dt), S_out / z_out device pointers (nullable),
- * as in la_causal_fwd. The heads are processed in up to four groups that
+ * as in la_causal_fwd. The heads are processed in groups (a quarter of them
+ * each, the last quarter split into all but four heads and four, so that
+ * little work is left after the last copy in) that
  * stream through two device staging buffers, so that copying a group in,
  * computing the previous one and copying the one before out overlap (separate
  * copy engines for the two directions). Each group is an la_causal_fwd call on

@@ -49,6 +49,16 @@ size_t elem_bytes(la_dtype dt) { return dt == LA_BF16 ? 2 : 4; }
 // group's slice of S_out and z_out stays 16-byte aligned.
 int64_t group_heads(int64_t BH) { return ((BH + kGroups - 1) / kGroups + 3) / 4 * 4; }
 
+// Heads of the group starting at head h0. The last full-size group is cut into
+// g - 4 and 4 heads: after the last copy in, only a 4-head forward and its copy
+// out remain, instead of a quarter of the batch (group starts stay multiples
+// of 4).
+int64_t group_size(int64_t BH, int64_t h0) {
+    const int64_t g = group_heads(BH), rest = BH - h0;
+    if (g >= 8 && rest > 4 && rest <= g) return rest - 4;
+    return rest < g ? rest : g;
+}
+
 }  // namespace
 
 extern "C" {
@@ -101,9 +111,9 @@ la_status la_causal_fwd_host(const void* q, const void* k, const void* v, void* 
     const char* hv = static_cast<const char*>(v);
     char* ho = static_cast<char*>(o);
     int g = 0;
-    for (int64_t h0 = 0; h0 < BH; h0 += g_heads, ++g) {
+    for (int64_t h0 = 0, nh = 0; h0 < BH; h0 += nh, ++g) {
         const int b = g & 1;
-        const int64_t nh = BH - h0 < g_heads ? BH - h0 : g_heads;
+        nh = group_size(BH, h0);
         char* buf = static_cast<char*>(staging) + b * buf_bytes;
         // Buffer b is free once the group two before has been copied out (which
         // itself waited for that group's compute).

@@ -1,6 +1,7 @@
 """la_causal_fwd_host: host q, k, v in, host o out, transfers overlapped.
 
-The heads go through the device in up to four groups; each group is an
+The heads go through the device in groups (a quarter of the heads each, the
+last quarter split into all but four heads and four); each group is an
 ordinary causal forward on its heads, so the output is checked against the
 float64 oracle with the gates of the device entry (row-wise relative error,
 1e-4 for float32 inputs, 2e-2 for bfloat16), and the final state against the
@@ -37,6 +38,7 @@ def rowwise_rel(got, ref):
     (1, 1, 129, 64, "bf16", True),     # a single head, one group
     (3, 3, 300, 32, "f32", True),      # fp32 SIMT path; groups of 4, 4, 1 heads
     (1, 6, 256, 64, "bf16", False),    # pageable host memory: correct, not overlapped
+    (4, 8, 300, 64, "bf16", True),     # groups of 8, 8, 8, 4, 4: the last group is split
 ])
 def test_host_entry_matches_oracle(la, B, H, N, D, dt, pinned):
     q, k, v = make_qkv(B, H, N, D, dt, seed=B * 1000 + H * 10 + N)
@@ -60,8 +62,9 @@ def test_host_entry_matches_oracle(la, B, H, N, D, dt, pinned):
         np.testing.assert_allclose(to_f64(z), zr, rtol=5e-3)
 
 
-def test_host_entry_equals_device_entry_fp32(la):
-    B, H, N, D = 2, 7, 333, 64
+@pytest.mark.parametrize("B,H", [(2, 7), (4, 8)])   # groups 4, 4, 4, 2 and 8, 8, 8, 4, 4
+def test_host_entry_equals_device_entry_fp32(la, B, H):
+    N, D = 333, 64
     q, k, v = (t.pin_memory() for t in make_qkv(B, H, N, D, "f32", seed=77))
     o_host = la.la_causal_fwd_host(q, k, v)
     dev = torch.device("cuda")
