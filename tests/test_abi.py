@@ -173,3 +173,37 @@ def test_layer_decode_workspace(lib):
     so = ctypes.CDLL(lib.library_path())
     n = ctypes.c_size_t(0)
     assert so.la_workspace_size(lib.LA_OP_LAYER_DECODE, B, H, 1, 64, 32, 1, ctypes.byref(n)) == 2
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    # A C caller (no C++, no CUDA headers) compiles against the header and links
+    # against the library: every entry point is taken by address, so a missing
+    # or mangled symbol fails the link.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    names = _declared()
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include "linattn.h"\n#include <stdio.h>\n'
+        "int main(void) {\n"
+        "    const void* fns[] = {" + ", ".join(f"(const void*)&{n}" for n in names) + "};\n"
+        '    size_t n = 0;\n'
+        '    la_status s = la_workspace_size(LA_OP_CAUSAL, 8, 8, 3072, 64, 64, LA_BF16, &n);\n'
+        '    printf("%d %zu %d\\n", (int)s, n, (int)(sizeof(fns) / sizeof(fns[0])));\n'
+        "    return s == LA_OK ? 0 : 1;\n}\n")
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(lib.library_path())
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                        str(src), "-L", libdir, "-llinattn", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    # Running it needs only the CUDA runtime to load; the size query touches no GPU.
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    status, size, count = r.stdout.split()
+    assert int(status) == 0 and int(size) == lib.la_workspace_size(lib.LA_OP_CAUSAL, 8, 8, 3072, 64, 64, lib.LA_BF16)
+    assert int(count) == len(names)
