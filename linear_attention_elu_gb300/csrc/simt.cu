@@ -1,4 +1,6 @@
-// SIMT (fp32 FMA) kernels for the causal and non-causal forward passes.
+// SIMT (fp32 FMA) kernels: the causal and non-causal forward passes, the
+// causal and non-causal backward, and the positive random features for the
+// shapes the tensor-core kernel does not take.
 //
 // These take any 1 <= Dk, Dv <= 128 and either input dtype, and compute in
 // fp32 throughout, so float32 inputs are never rounded to a tensor-core
@@ -14,7 +16,9 @@
 // into whole chunks plus a masked in-chunk part; the prefix over chunks is
 // the parallel scan the same blog names in section 7.7.
 // Non-causal evaluation splits the sequence, reduces the partial S, z
-// (section 6.2's boxed S and z) and applies them to every query.
+// (section 6.2's boxed S and z) and applies them to every query. For
+// Dk, Dv <= 64 the chunk products run in the register-tiled kernels further
+// down (the same sums in the same order); the general kernels take the rest.
 #include "common.cuh"
 #include "kernels.h"
 
