@@ -9,8 +9,8 @@
 
 namespace la {
 
-// Every launcher takes `fm`, the feature map (the la_phi values: kPhiElu1 or
-// kPhiIdentity, defined in common.cuh).
+// The attention launchers take `fm`, the feature map (the la_phi values:
+// kPhiElu1 or kPhiIdentity, defined in common.cuh).
 
 // fp32-arithmetic SIMT paths (any 1 <= D, M <= 128, either dtype).
 size_t simt_causal_workspace(int64_t BH, int N, int D, int M);
