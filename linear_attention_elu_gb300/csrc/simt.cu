@@ -27,7 +27,7 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kScanBatch = 8;  // chunks per batch of loads in the chunk scans
+constexpr int kScanBatch = 16;  // chunks per batch of loads in the chunk scans
 
 template <typename T>
 __device__ __forceinline__ void load_rows_phi(float* dst, int ld, const T* src, int rows,
