@@ -59,6 +59,14 @@ cublasStatus_t make_plan(cublasLtHandle_t h, int rows, int K, int N, la_dtype dt
     const size_t ws = kLtWorkspace;
     s = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws,
                                              sizeof(ws));
+    // The entry point guarantees 16-byte alignment only (the heuristic's default
+    // assumption is 256): exclude algorithms that need more.
+    const uint32_t align = 16;
+    const cublasLtMatmulPreferenceAttributes_t align_attr[4] = {
+        CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES,
+        CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES};
+    for (int a = 0; a < 4 && s == CUBLAS_STATUS_SUCCESS; ++a)
+        s = cublasLtMatmulPreferenceSetAttribute(pref, align_attr[a], &align, sizeof(align));
     cublasLtMatmulHeuristicResult_t res = {};
     int found = 0;
     if (s == CUBLAS_STATUS_SUCCESS)

@@ -61,6 +61,29 @@ def test_layer_steps_match_oracle(la, B, H, D, dt, steps):
     assert rel.max() <= (1e-5 if dt == "f32" else 1e-2)
 
 
+def test_layer_with_16_byte_aligned_buffers(la):
+    # x and y 16 bytes past a 256-byte boundary: the entry point promises 16-byte
+    # alignment, so the projections must not assume more.
+    B, H, D = 64, 8, 64
+    dm = H * D
+    Wqkv, Wo = weights(dm, "bf16", seed=3)
+    x = make_qkv(1, 1, B, dm, "bf16", seed=4)[2][0, 0]
+    dev = torch.device("cuda")
+    xbuf = torch.zeros(B * dm + 8, dtype=torch.bfloat16, device=dev)
+    ybuf = torch.zeros(B * dm + 8, dtype=torch.bfloat16, device=dev)
+    xs = xbuf[8:].view(B, dm)
+    ys = ybuf[8:].view(B, dm)
+    xs.copy_(x.to(dev))
+    assert xs.data_ptr() % 256 == 16 and ys.data_ptr() % 256 == 16
+    S = torch.zeros(B, H, D, D, device=dev)
+    z = torch.zeros(B, H, D, device=dev)
+    la.la_layer_decode_step(xs, Wqkv.to(dev), Wo.to(dev), S, z, H, y=ys)
+    torch.cuda.synchronize()
+    Sr, zr = np.zeros((B, H, D, D)), np.zeros((B, H, D))
+    ref = layer.layer_decode_step(to_f64(x), to_f64(Wqkv), to_f64(Wo), Sr, zr, H)
+    assert rowwise_rel(to_f64(ys), ref) <= TOL["bf16"]
+
+
 def test_layer_rejects_mismatched_heads(la):
     with pytest.raises(ValueError):
         la.la_layer_decode_step(torch.zeros(2, 100, device="cuda", dtype=torch.bfloat16),
