@@ -8,6 +8,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionstart(session):
+    # The library under test is built in-tree. Build it (or rebuild it after a
+    # source change) before collection, so that a fresh checkout tests the code it
+    # ships; when it is up to date this does nothing.
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_la_build", os.path.join(ROOT, "linear_attention_elu_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    if not mod.up_to_date():
+        mod.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 
