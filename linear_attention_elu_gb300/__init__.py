@@ -23,7 +23,7 @@ __all__ = [
     "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
     "la_causal_bwd", "LA_OP_CAUSAL_BWD", "la_noncausal_bwd", "LA_OP_NONCAUSAL_BWD",
     "LA_PHI_ELU1", "LA_PHI_IDENTITY", "la_positive_random_features", "LA_OP_LAYER_DECODE",
-    "la_layer_decode_step", "library_path",
+    "la_layer_decode_step", "la_causal_fwd_noalloc", "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
@@ -92,6 +92,8 @@ def _load():
     lib.la_noncausal_bwd_phi.restype = I
     lib.la_positive_random_features.argtypes = [P, P, P, L, I, I, I, F, P]
     lib.la_positive_random_features.restype = I
+    lib.la_causal_fwd_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P]
+    lib.la_causal_fwd_noalloc.restype = I
     lib.la_layer_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     lib.la_layer_decode_step.restype = I
     lib.la_query_status.argtypes = [P, P]
@@ -238,6 +240,22 @@ def _causal_phi(q, k, v, S0, z0, o, eps, S_out, z_out, ws, stream, phi):
                                   int(phi), float(eps), _ptr(S0), _ptr(z0), _ptr(S_out),
                                   _ptr(z_out), _ptr(ws), ws.numel(), _stream(stream)),
            "la_causal_fwd_phi")
+    return o
+
+
+def la_causal_fwd_noalloc(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, stream=None):
+    """la_causal_fwd without a workspace (scratch is a fixed array inside the library)."""
+    B, H, N, Dk, Dv = _shape4(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _need_cuda(q, k, v, o, S_out, z_out)
+    for t, shp in ((S_out, (B, H, Dk, Dv)), (z_out, (B, H, Dk))):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
+            raise ValueError(f"state outputs must be float32 with shape {shp}")
+    _check(_lib.la_causal_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv,
+                                      _dt(q), float(eps), _ptr(S_out), _ptr(z_out),
+                                      _stream(stream)),
+           "la_causal_fwd_noalloc")
     return o
 
 

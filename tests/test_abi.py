@@ -207,3 +207,21 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     status, size, count = r.stdout.split()
     assert int(status) == 0 and int(size) == lib.la_workspace_size(lib.LA_OP_CAUSAL, 8, 8, 3072, 64, 64, lib.LA_BF16)
     assert int(count) == len(names)
+
+
+def test_binding_sets_a_signature_for_every_declared_function(lib):
+    # A function called through ctypes without argtypes would pass every
+    # argument as a C int: the binding must declare each one.
+    with open(os.path.join(ROOT, "linear_attention_elu_gb300", "__init__.py")) as f:
+        text = f.read()
+    bound = set(re.findall(r"lib\.(la_[a-z0-9_]+)\.argtypes", text))
+    missing = sorted(set(_declared()) - bound)
+    assert not missing, missing
+
+
+def test_wrappers_refuse_host_tensors_before_any_launch(lib):
+    import torch
+    q = torch.zeros(1, 1, 4, 64)
+    for fn in (lib.la_causal_fwd, lib.la_noncausal_fwd, lib.la_causal_fwd_noalloc):
+        with pytest.raises(ValueError):
+            fn(q, q, q)
