@@ -1,9 +1,11 @@
 """Benchmark: causal linear-attention forward (phi = elu + 1) tokens/s on GB300.
 
 One step = one la_causal_fwd call (every kernel of the causal path) over one
-batch of the causal B=8 H=8 N=3072 D=64 bf16 workload (a 32x32x3 pixel-channel
-sequence), inputs resident in device memory. Input sets rotate so that the
-bytes touched between two reads of one set exceed the L2 cache.
+batch of the long-context causal workload B=2 H=8 N=65536 D=64 bf16 (k scaled
+by 1/8), the largest causal configuration, inputs resident in device memory.
+Input sets rotate so that the bytes touched between two reads of one set
+exceed the L2 cache. `--workload image` times the B=8 H=8 N=3072 shape (a
+32x32x3 pixel-channel sequence) instead; it is also reported under `also`.
 
 Prints ONE JSON line (rank 0). `--impl reference` times the float64 CPU
 oracle on the same workload instead (a deliberately slow baseline).
@@ -39,7 +41,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="image", choices=["image", "long"])
+    p.add_argument("--workload", default="long", choices=["image", "long"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-also", action="store_true",
@@ -258,10 +260,49 @@ NC_BWD_MACS_PER_TOKEN_D64 = 4160 + 8320 + 12352
 FP32_FMA_PEAK = 152 * 128 * 2 * 2.07e9
 
 
-def other_paths(la, dev, stream):
-    """Secondary measurements of the other two operations of the path."""
+def causal_also(la, w, dev, stream, calls=100):
+    """The causal forward on another workload: rotating input sets larger than L2,
+    one graph of `calls` consecutive calls, CUDA events around its replay."""
+    hbm, _ = peaks()
+    per_set = alg_bytes(w)
+    R = max(2, -(-3 * L2_BYTES // per_set) + 1)
+    sets = []
+    for r in range(R):
+        q, k, v = make_workload(w, seed=r)
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(v, device=dev)))
+    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, sets[0][0].dtype, dev)
+    for i in range(3):
+        q, k, v, o = sets[i % R]
+        la.la_causal_fwd(q, k, v, o=o, ws=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(calls):
+            q, k, v, o = sets[i % R]
+            la.la_causal_fwd(q, k, v, o=o, ws=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / calls
+    gbps = alg_bytes(w) / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_call": ms,
+            "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s",
+                         "frac": gbps / hbm},
+            "l2": f"{R} rotating input sets of {per_set / 1e6:.1f} MB",
+            "status": la.la_query_status(ws)}
+
+
+def other_paths(la, dev, stream, main_workload):
+    """Secondary measurements: the other causal shape and the other operations of the path."""
     hbm, _ = peaks()
     out = {}
+    other = "image" if main_workload == "long" else "long"
+    out[other] = causal_also(la, WORKLOADS[other], dev, stream, calls=200 if other == "image" else 20)
     # Non-causal, B=16 H=8 N=8192 D=128 bf16 (one 1.07 GB input set, larger than L2).
     w = WORKLOADS["bidir"]
     gen = torch.Generator(device=dev)
@@ -292,38 +333,83 @@ def other_paths(la, dev, stream):
                         "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm,
                         "status": la.la_query_status(ws)}
     del q, k, v, o, ws, g
-    # Decode, 512 sequences x 8 heads, D=64: 256 consecutive steps in one graph.
-    w = WORKLOADS["decode"]
-    T = 256
-    q, k, v = (torch.randn(T, w.B, w.H, w.D, device=dev, generator=gen).bfloat16()
-               for _ in range(3))
-    o = torch.empty_like(v)
-    S = torch.zeros(w.B, w.H, w.D, w.D, device=dev)
-    z = torch.zeros(w.B, w.H, w.D, device=dev)
-
-    def steps():
-        for t in range(T):
-            la.la_decode_step(q[t], k[t], v[t], S, z, o=o[t])
-
-    steps()
-    torch.cuda.synchronize()
+    # L2 reference for the decode step, whose fp32 state stays in L2 between steps:
+    # an in-place scale of a 64 MB fp32 buffer (each byte read and written at the
+    # same address, as the decode step does with S and z), 200 launches in one graph.
+    x = torch.ones(16 * 2 ** 20, device=dev)
     g = torch.cuda.CUDAGraph()
+    x.mul_(1.0)
+    torch.cuda.synchronize()
     with torch.cuda.graph(g):
+        for _ in range(200):
+            x.mul_(1.0)
+    best = None
+    for _ in range(3):
+        g.replay()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / 200
+        best = t if best is None else min(best, t)
+    l2_gbps = 2 * x.numel() * 4 / (best * 1e-3) / 1e9
+    out["l2_peak"] = {"GBps": l2_gbps, "how": "torch in-place x.mul_(1.0) over a 64 MB fp32 "
+                      "buffer (read + write, L2-resident), 200 launches in one CUDA graph, best of 3"}
+    del x, g
+
+    def decode_run(B, T):
+        """us per step of T consecutive decode steps in one graph (B sequences x 8 heads)."""
+        w = WORKLOADS["decode"]
+        q, k, v = (torch.randn(T, B, w.H, w.D, device=dev, generator=gen).bfloat16()
+                   for _ in range(3))
+        o = torch.empty_like(v)
+        S = torch.zeros(B, w.H, w.D, w.D, device=dev)
+        z = torch.zeros(B, w.H, w.D, device=dev)
+
+        def steps():
+            for t in range(T):
+                la.la_decode_step(q[t], k[t], v[t], S, z, o=o[t])
+
         steps()
-    g.replay()
-    torch.cuda.synchronize()
-    a.record(stream)
-    g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) / T * 1e3
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            steps()
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / T * 1e3
+
+    # Decode, 512 sequences x 8 heads, D=64: all 3072 steps of the configuration in one
+    # graph. The 68 MB fp32 state stays in the 129 MB L2 between steps, so its
+    # roofline is the L2 read+write rate above.
+    w = WORKLOADS["decode"]
+    us = decode_run(w.B, w.N)
     per_step = 33792 * w.B * w.H
-    out["decode"] = {"workload": w.name.replace("3072 steps", f"{T} steps timed"),
-                     "value": 1e6 / us, "unit": "steps/s", "us_per_step": us,
-                     "alg_GBps": per_step / (us * 1e-6) / 1e9,
-                     "frac_of_hbm": per_step / (us * 1e-6) / 1e9 / hbm,
+    gbps = per_step / (us * 1e-6) / 1e9
+    out["decode"] = {"workload": w.name + ", all steps timed", "value": 1e6 / us,
+                     "unit": "steps/s", "us_per_step": us, "alg_GBps": gbps,
+                     "roofline": {"bound": "l2", "achieved": gbps, "peak": l2_gbps,
+                                  "unit": "GB/s", "frac": gbps / l2_gbps,
+                                  "peak_source": "l2_peak (measured in this run)"},
+                     "frac_of_hbm": gbps / hbm,
                      "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
-    del q, k, v, o, S, z, g
+    # The same step with 2048 sequences x 8 heads: 272 MB of fp32 state, larger than
+    # L2, so every step streams it from and to HBM.
+    Bbig, Tbig = 2048, 256
+    us_big = decode_run(Bbig, Tbig)
+    per_big = 33792 * Bbig * w.H
+    gbps_big = per_big / (us_big * 1e-6) / 1e9
+    out["decode_2048"] = {"workload": f"decode {Bbig} seq x H=8 D=64 bf16, fp32 state 272 MB, "
+                                      f"{Tbig} steps timed",
+                          "value": 1e6 / us_big, "unit": "steps/s", "us_per_step": us_big,
+                          "alg_GBps": gbps_big,
+                          "roofline": {"bound": "hbm", "achieved": gbps_big, "peak": hbm,
+                                       "unit": "GB/s", "frac": gbps_big / hbm}}
+    T = 256
     # Layer decode step at the same batch (512 sequences, d_model = 8 x 64, bf16,
     # synthetic weights): QKV projection, the decode step, output projection.
     dm = w.H * w.D
@@ -599,7 +685,7 @@ def main():
     d2h = ho.numel() * ho.element_size()
     del sets, graphs, g_warm, g_timed
 
-    also = {} if args.no_also else other_paths(la, dev, stream)
+    also = {} if args.no_also else other_paths(la, dev, stream, args.workload)
 
     hbm, src = peaks()
     # Average launch duration over the timed region (events around the K steps);

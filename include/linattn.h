@@ -221,12 +221,39 @@ la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void*
  *  - All calls share the one array, which keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, or concurrent host
  *    threads without ordering) race on it and must be serialised by the caller.
- *  - Device-side wait timeouts are recorded in the array's header, which the
- *    caller cannot query.
+ *    A bf16 call that follows an fp32 call on the same device first clears the
+ *    part of the array it reads (cudaMemsetAsync on `stream`), so the fp32
+ *    path's per-chunk states are never taken for the bf16 path's tagged sums.
+ *  - The array used is the current device's: `stream` (unless it is a default
+ *    stream) and every pointer must belong to that device, else
+ *    LA_ERR_INVALID_ARG (checked with cudaStreamGetDevice and
+ *    cudaPointerGetAttributes before any launch).
+ *  - Device-side wait timeouts are recorded in the array's header:
+ *    la_noalloc_query_status reads and clears that status.
  */
 la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
                                 int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
                                 float* S_out, float* z_out, la_stream_t stream);
+
+/*
+ * Status of the la_causal_fwd_noalloc calls on the current device, as
+ * la_query_status gives it for a workspace: synchronises `stream`, returns the
+ * first device-side error recorded since the last query (LA_ERR_TIMEOUT when
+ * a bounded wait ran out and the output is incomplete) and clears it; LA_OK
+ * when none was recorded or no call has run on this device yet. No
+ * counterpart in the paper: it reports on the library's own array.
+ */
+la_status la_noalloc_query_status(la_stream_t stream);
+
+/*
+ * Wait limit of the la_causal_fwd_noalloc calls on the current device, in
+ * microseconds (0 restores the default of 2 s), and a test hook: hold_loads
+ * != 0 makes the tensor-core path withhold its input loads so that its waits
+ * run out (used to test failure detection without a GPU fault; 0 in normal
+ * use). Written into the array's header by a one-thread kernel on `stream`,
+ * so it applies to the calls queued after it. No counterpart in the paper.
+ */
+la_status la_noalloc_set_wait_limit(unsigned int max_spin_us, int hold_loads, la_stream_t stream);
 
 /*
  * Causal forward on HOST buffers: q, k, v, o are host pointers in the layout of

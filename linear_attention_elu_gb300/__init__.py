@@ -23,7 +23,8 @@ __all__ = [
     "la_host_staging_size", "host_staging", "la_causal_fwd_host", "la_causal_fwd_state",
     "la_causal_bwd", "LA_OP_CAUSAL_BWD", "la_noncausal_bwd", "LA_OP_NONCAUSAL_BWD",
     "LA_PHI_ELU1", "LA_PHI_IDENTITY", "la_positive_random_features", "LA_OP_LAYER_DECODE",
-    "la_layer_decode_step", "la_causal_fwd_noalloc", "library_path",
+    "la_layer_decode_step", "la_causal_fwd_noalloc", "la_noalloc_query_status",
+    "la_noalloc_set_wait_limit", "library_path",
 ]
 
 LA_F32, LA_BF16 = 0, 1
@@ -94,6 +95,10 @@ def _load():
     lib.la_positive_random_features.restype = I
     lib.la_causal_fwd_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P]
     lib.la_causal_fwd_noalloc.restype = I
+    lib.la_noalloc_query_status.argtypes = [P]
+    lib.la_noalloc_query_status.restype = I
+    lib.la_noalloc_set_wait_limit.argtypes = [ctypes.c_uint, I, P]
+    lib.la_noalloc_set_wait_limit.restype = I
     lib.la_layer_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     lib.la_layer_decode_step.restype = I
     lib.la_query_status.argtypes = [P, P]
@@ -244,7 +249,10 @@ def _causal_phi(q, k, v, S0, z0, o, eps, S_out, z_out, ws, stream, phi):
 
 
 def la_causal_fwd_noalloc(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, stream=None):
-    """la_causal_fwd without a workspace (scratch is a fixed array inside the library)."""
+    """la_causal_fwd without a workspace (scratch is a fixed array inside the library).
+
+    The library uses the array of the current device, so the call runs with
+    q's device current."""
     B, H, N, Dk, Dv = _shape4(q, k, v)
     if o is None:
         o = torch.empty_like(v)
@@ -252,11 +260,27 @@ def la_causal_fwd_noalloc(q, k, v, o=None, eps=1e-6, S_out=None, z_out=None, str
     for t, shp in ((S_out, (B, H, Dk, Dv)), (z_out, (B, H, Dk))):
         if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != shp):
             raise ValueError(f"state outputs must be float32 with shape {shp}")
-    _check(_lib.la_causal_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv,
-                                      _dt(q), float(eps), _ptr(S_out), _ptr(z_out),
-                                      _stream(stream)),
-           "la_causal_fwd_noalloc")
+    with torch.cuda.device(q.device):
+        _check(_lib.la_causal_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, Dk, Dv,
+                                          _dt(q), float(eps), _ptr(S_out), _ptr(z_out),
+                                          _stream(stream)),
+               "la_causal_fwd_noalloc")
     return o
+
+
+def la_noalloc_query_status(device=None, stream=None):
+    """Reads and clears the device-side status of the no-allocation calls on `device`."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return _lib.la_noalloc_query_status(_stream(stream))
+
+
+def la_noalloc_set_wait_limit(max_spin_us=0, hold_loads=False, device=None, stream=None):
+    """Wait limit (microseconds, 0 = default) and load-withholding test hook of the
+    no-allocation calls on `device`."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(_lib.la_noalloc_set_wait_limit(int(max_spin_us), 1 if hold_loads else 0,
+                                              _stream(stream)),
+               "la_noalloc_set_wait_limit")
 
 
 def la_causal_fwd_state(q, k, v, S0, z0, o=None, eps=1e-6, S_out=None, z_out=None, ws=None,
