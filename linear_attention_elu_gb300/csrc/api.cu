@@ -45,7 +45,7 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
             if (la::tc_causal_supported(Dk, Dv, dt)) return la::tc_causal_workspace(BH, N);
             return la::simt_causal_workspace(BH, N, Dk, Dv);
         case LA_OP_NONCAUSAL:
-            if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N);
+            if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N, Dk);
             return la::simt_noncausal_workspace(BH, N, Dk, Dv);
         case LA_OP_CAUSAL_BWD:
         case LA_OP_NONCAUSAL_BWD:
@@ -232,7 +232,7 @@ la_status la_noncausal_fwd_phi(const void* q, const void* k, const void* v, void
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
     if (la::tc_noncausal_supported(Dk, Dv, dt))
-        return from_cuda(la::tc_noncausal(q, k, v, o, BH, N, eps, phi, workspace, body,
+        return from_cuda(la::tc_noncausal(q, k, v, o, BH, N, Dk, eps, phi, workspace, body,
                                           (cudaStream_t)stream));
     return from_cuda(la::simt_noncausal(q, k, v, o, dt, BH, N, Dk, Dv, eps, phi, body,
                                         (cudaStream_t)stream));

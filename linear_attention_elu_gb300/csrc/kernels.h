@@ -52,9 +52,9 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
 
 // Tensor-core (tcgen05) non-causal path: bf16, Dk = Dv = 128.
 bool tc_noncausal_supported(int D, int M, la_dtype dt);
-size_t tc_noncausal_workspace(int64_t BH, int N);
+size_t tc_noncausal_workspace(int64_t BH, int N, int D);
 cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                         float eps, int fm, void* ws_header, void* scratch, cudaStream_t st);
+                         int D, float eps, int fm, void* ws_header, void* scratch, cudaStream_t st);
 
 // Decode step (SIMT, bandwidth bound).
 cudaError_t decode_step(const void* q, const void* k, const void* v, void* o, float* S, float* z,

@@ -60,7 +60,8 @@ def test_causal_identity_map(la, B, H, N, C, M, dt):
 
 
 @pytest.mark.parametrize("B,H,N,C,M,dt", [
-    (2, 2, 1000, 128, 128, "bf16"),  # tensor-core non-causal path
+    (2, 2, 1000, 128, 128, "bf16"),  # tensor-core non-causal path, D = 128
+    (2, 2, 1000, 64, 64, "bf16"),    # tensor-core non-causal path, D = 64
     (1, 3, 300, 64, 48, "f32"),      # fp32 SIMT tiled
     (1, 2, 150, 96, 64, "bf16"),     # SIMT general path
 ])

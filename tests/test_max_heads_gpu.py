@@ -38,7 +38,8 @@ def sampled(t):
 @pytest.mark.parametrize("causal,dt,N", [
     (True, "bf16", 3),       # tensor-core causal: ~431 one-chunk heads per CTA range
     (True, "f32", 3),        # fp32 path: grid.y = 65535
-    (False, "bf16", 3),      # non-causal at D = 64: fp32-arithmetic kernels
+    (False, "bf16", 3),      # non-causal at D = 64: tensor-core pair, one-chunk heads
+    (False, "f32", 3),       # non-causal fp32 path
 ])
 def test_forward_at_maximum_head_count(la, causal, dt, N):
     q, k, v = make_qkv(B, H, N, 64, dt, seed=N)

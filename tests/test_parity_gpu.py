@@ -292,9 +292,10 @@ def test_tc_causal_long_config_rows_sampled_against_quadratic(la):
 # ------------------------------------------------------------ tensor-core non-causal path
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 1, 128), (1, 1, 129), (2, 3, 1000),
                                    (1, 2, 20000), (3, 5, 777), (40, 8, 256)])
-def test_tc_noncausal_partitions(la, B, H, N):
-    q, k, v = make_qkv(B, H, N, 128, "bf16", seed=B * 100 + H * 10 + N + 7)
+def test_tc_noncausal_partitions(la, B, H, N, D):
+    q, k, v = make_qkv(B, H, N, D, "bf16", seed=B * 100 + H * 10 + N + 7 + D)
     err = rowwise_rel(run(la, "noncausal", q, k, v), ref("noncausal", q, k, v))
     assert err <= TOL["bf16"], err

@@ -46,11 +46,12 @@ def test_withheld_load_times_out_and_context_survives(la):
     assert err <= 2e-2
 
 
-def test_withheld_load_times_out_noncausal(la):
+@pytest.mark.parametrize("D", [64, 128])
+def test_withheld_load_times_out_noncausal(la, D):
     dev = torch.device("cuda")
-    q, k, v = make_qkv(1, 4, 700, 128, "bf16", seed=4)
+    q, k, v = make_qkv(1, 4, 700, D, "bf16", seed=4)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    ws = la.workspace(la.LA_OP_NONCAUSAL, 1, 4, 700, 128, 128, torch.bfloat16, dev)
+    ws = la.workspace(la.LA_OP_NONCAUSAL, 1, 4, 700, D, D, torch.bfloat16, dev)
     hdr = ws[:256].view(torch.int32)
     hdr[MAX_SPIN_WORD] = 2000  # 2 ms
     hdr[HOLD_WORD] = 1
