@@ -478,7 +478,8 @@ def other_paths(la, dev, stream, main_workload):
         "value": 1e6 / lus, "unit": "steps/s", "us_per_step": lus,
         "attention_share_est": us / lus,
         "projection_tflops_if_rest": gemm_flops / max(lus - us, 1e-3) / 1e6,
-        "note": "projections are cuBLASLt bf16 GEMMs; the decode step between them is ours"}
+        "note": "projections: the library's tcgen05 bf16 products (128 x 64 tiles); "
+                "the decode step between them is the library's decode kernel"}
     del Wqkv, Wo, xs, ys, S, z, ws, g
     # Causal and non-causal forward on fp32 inputs (the fp32 SIMT path) at the
     # image shape B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.

@@ -353,12 +353,14 @@ la_status la_positive_random_features(const void* x, const void* W, void* out, i
  *    all row-major, dtype dt, device pointers, 16-byte aligned.
  *  - S: [B, H, D, D], z: [B, H, D] float32, read and written in place.
  *  - workspace: la_workspace_size(LA_OP_LAYER_DECODE, B, H, 1, D, D, dt, ...)
- *    bytes (the projection buffers and cuBLASLt scratch), 256-byte aligned.
- *  - The projections are cuBLASLt GEMMs with fp32 accumulation (the library's
- *    one dependency beyond the CUDA runtime); the step between them is this
- *    library's decode kernel, reading q, k, v in place in the projection. The
- *    three launches go to `stream`; la_launch_count counts the library's own
- *    kernel (1).
+ *    bytes (a header and the projection buffers), 256-byte aligned, zeroed
+ *    once by la_workspace_init; la_query_status reports a projection whose
+ *    bounded waits ran out.
+ *  - The projections are this library's products with fp32 accumulation
+ *    (tcgen05 tensor cores for bf16 when d_model is a multiple of 8, fp32 FMA
+ *    otherwise); the step between them is its decode kernel, reading q, k, v
+ *    in place in the projection. The three launches go to `stream`;
+ *    la_launch_count gives 3.
  */
 la_status la_layer_decode_step(const void* x, const void* Wqkv, const void* Wo, void* y,
                                float* S, float* z, int B, int H, int D, la_dtype dt, float eps,

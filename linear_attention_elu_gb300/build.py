@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", *objs, "-lcublasLt", "-o", tmp]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -184,7 +184,9 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
         *launches = 0;
         return LA_OK;
     }
-    if (one_token)
+    if (op == LA_OP_LAYER_DECODE)
+        *launches = 3;                           // two projections and the decode step
+    else if (one_token)
         *launches = 1;
     else if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD)
         *launches = 5;

@@ -43,6 +43,10 @@ __global__ void __launch_bounds__(256, 4) decode64_kernel(const T* __restrict__ 
                                                        float eps, int H, int64_t ld_qk,
                                                        int64_t ld_v) {
     constexpr int fm = kFm;
+    // When launched as a programmatic dependent (the layer step), the inputs
+    // come from the kernel before: wait for it (a no-op otherwise).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t h = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (h >= BH) return;
@@ -150,6 +154,20 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* o, 
     if (D == 64 && M == 64) {
         const int heads_per_block = 8;
         const int64_t blocks = (BH + heads_per_block - 1) / heads_per_block;
+        if (H > 1) {
+            // The layer step: a programmatic dependent of the projection before it.
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)blocks);
+            cfg.blockDim = dim3(256);
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, decode64_kernel<T, kFm>, (const T*)q, (const T*)k,
+                                      (const T*)v, (T*)o, S, z, BH, eps, H, ld_qk, ld_v);
+        }
         decode64_kernel<T, kFm><<<(unsigned)blocks, 256, 0, st>>>(
             (const T*)q, (const T*)k, (const T*)v, (T*)o, S, z, BH, eps, H, ld_qk, ld_v);
     } else {

@@ -69,4 +69,11 @@ cudaError_t decode_step_strided(const void* q, const void* k, const void* v, voi
 // Layer decode step (csrc/layer.cu): workspace bytes after the header.
 size_t layer_workspace(int B, int H, int D, la_dtype dt);
 
+// Y = X W, row-major X [rows, K], W [K, N], Y [rows, N], fp32 accumulation
+// (csrc/gemm.cu): tcgen05 for bf16 with K, N multiples of 8, fp32 FMA otherwise.
+// A bounded wait that runs out is recorded in the header at ws_header.
+bool gemm_uses_tensor_cores(int K, int N, la_dtype dt);
+cudaError_t gemm(const void* X, const void* W, void* Y, int rows, int K, int N, la_dtype dt,
+                 void* ws_header, cudaStream_t st);
+
 }  // namespace la

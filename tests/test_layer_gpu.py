@@ -40,7 +40,9 @@ def weights(dm, dt, seed):
 @pytest.mark.parametrize("B,H,D,dt,steps", [
     (512, 8, 64, "bf16", 4),     # the blog's layer shape, batch of 512 sequences
     (7, 3, 32, "f32", 5),        # odd batch, generic decode kernel
-    (16, 2, 48, "bf16", 3),
+    (16, 2, 48, "bf16", 3),      # tensor-core products with K and N tails (d_model 96)
+    (300, 4, 40, "bf16", 2),     # three row tiles, the last partial (d_model 160)
+    (5, 3, 5, "bf16", 3),        # d_model 15: rows not 16-byte multiples, fp32-FMA products
 ])
 def test_layer_steps_match_oracle(la, B, H, D, dt, steps):
     dm = H * D
