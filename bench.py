@@ -180,6 +180,39 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def host_numa(device_index, host_ptr):
+    """NUMA placement of the e2e path: the GPU's node (from its PCI device) and the
+    nodes holding the pages of a pinned host buffer (from /proc/self/numa_maps)."""
+    out = {"cpus": len(os.sched_getaffinity(0))}
+    try:
+        props = torch.cuda.get_device_properties(device_index)
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            out["gpu_numa_node"] = int(f.read().strip())
+        out["gpu_pci"] = bus
+    except Exception:  # noqa: BLE001
+        out["gpu_numa_node"] = None
+    try:
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                addr = int(line.split()[0], 16)
+                # numa_maps lists each mapping by its start address; the buffer's
+                # mapping is the last one that starts at or below it.
+                if addr <= host_ptr:
+                    best = line
+                else:
+                    break
+        nodes = {}
+        for tok in best.split()[1:]:
+            if tok.startswith("N") and "=" in tok:
+                n, c = tok[1:].split("=")
+                nodes[int(n)] = int(c)
+        out["pinned_buffer_pages_by_node"] = nodes
+    except Exception:  # noqa: BLE001
+        out["pinned_buffer_pages_by_node"] = None
+    return out
+
+
 def cpu_baseline(w, budget_s=10.0):
     """Times the float64 oracle (recurrent form) on whole heads of the workload."""
     import oracle
@@ -716,6 +749,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = job_ms(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
+    numa = host_numa(local, hq.data_ptr())
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size()
     del sets, graphs, g_warm, g_timed
@@ -745,7 +779,7 @@ def main():
                      "avg_launch_ms_timed": launch_ms,
                      "isolated_call_ms": call_ms},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "host_numa": numa},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "submission": {"timed": "one CUDA graph of the K steps, replayed once",
