@@ -86,6 +86,15 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:  # noqa: BLE001
+        return 1900.0
+
+
 def alg_bytes(w):
     """Algorithmic bytes of one forward: read q, k, v and write o once."""
     elem = 2 if w.dtype == "bf16" else 4
@@ -283,6 +292,18 @@ def run_reference(args, w):
 # 4,160; rows 8,320 (den 64, num 4,096, reverse sum 4,160); gradients 12,352
 # (dq 4,096 + 64, dk 4,096, dv 4,096).
 BWD_MACS_PER_TOKEN_D64 = 4160 + 12513 + 24832
+# Multiply-adds the tensor-core backward issues per token (bf16, Dk = Dv = 64,
+# 128-token chunks, MMA shapes as executed). Causal: chunk state [V | 1]^T phi(K)
+# 64 x 128 = 8,192; rows pass: phi(Q) phi(K)^T 128 x 64 = 8,192, P [V | 1]
+# 80 x 128 = 10,240, phi(Q) [S^T | z] 80 x 64 = 5,120, [dnum | dd]^T phi(Q)
+# 64 x 128 = 8,192; gradient pass: G and W 2 x 8,192, and each of dphi(q),
+# dphi(k), dv 64 x 64 + 64 x 128 = 12,288. Non-causal: state 8,192; rows 5,120 +
+# 8,192; gradients 3 x 4,096.
+TC_BWD_MACS_PER_TOKEN_D64 = 8192 + 8192 + 10240 + 5120 + 8192 + 2 * 8192 + 3 * 12288
+TC_NC_BWD_MACS_PER_TOKEN_D64 = 8192 + 5120 + 8192 + 3 * 4096
+# Bytes a backward pass must move per token at D = 64 bf16: q, k, v, dout read,
+# dq, dk, dv written.
+BWD_ALG_BYTES_PER_TOKEN_D64 = 7 * 64 * 2
 # The fp32 causal forward per token at Dk = Dv = 64: chunk state 4,160; output
 # A 2,080, den 64, A V 2,080, phi(q) S_prev 4,096.
 FWD_F32_MACS_PER_TOKEN_D64 = 4160 + 2080 + 64 + 2080 + 4096
@@ -546,16 +567,16 @@ def other_paths(la, dev, stream, main_workload):
                     "bound": "alu (fp32 FMA)"}
         del ws, g
     del q, k, v, o
-    # Causal and non-causal backward (fp32 SIMT arithmetic) at the image shape
-    # B=8 H=8 N=3072 D=64 bf16.
+    # Causal and non-causal backward (tensor-core kernels for bf16 D = 64) at the
+    # image shape B=8 H=8 N=3072 D=64 bf16.
     q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
                      for _ in range(4))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     for key, fn, op, macs, name in (
-            ("causal_bwd", la.la_causal_bwd, la.LA_OP_CAUSAL_BWD, BWD_MACS_PER_TOKEN_D64,
+            ("causal_bwd", la.la_causal_bwd, la.LA_OP_CAUSAL_BWD, TC_BWD_MACS_PER_TOKEN_D64,
              w.name.replace("causal", "causal backward")),
             ("noncausal_bwd", la.la_noncausal_bwd, la.LA_OP_NONCAUSAL_BWD,
-             NC_BWD_MACS_PER_TOKEN_D64, w.name.replace("causal", "non-causal backward"))):
+             TC_NC_BWD_MACS_PER_TOKEN_D64, w.name.replace("causal", "non-causal backward"))):
         ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
         fn(q, k, v, dout, dq, dk, dv, ws=ws)
         torch.cuda.synchronize()
@@ -572,10 +593,13 @@ def other_paths(la, dev, stream, main_workload):
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / reps
         flops = w.tokens * 2 * macs
+        gbps = w.tokens * BWD_ALG_BYTES_PER_TOKEN_D64 / (ms * 1e-3) / 1e9
         out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
-                    "ms_per_call": ms, "tflops": flops / (ms * 1e-3) / 1e12,
-                    "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
-                    "bound": "alu (fp32 FMA)"}
+                    "ms_per_call": ms, "tflops_executed": flops / (ms * 1e-3) / 1e12,
+                    "frac_of_bf16_dense": flops / (ms * 1e-3) / 1e12 / bf16_peak(),
+                    "alg_GBps": gbps, "frac_of_hbm": gbps / hbm,
+                    "bound": "latency: one CTA per 128-token chunk runs load, MMAs and "
+                             "epilogue in sequence (neither pipe nor DRAM saturated)"}
         del ws, g
     # Positive random features (R = 64, x scaled by D^-1/4) of q and k, then the
     # identity-map causal forward on the tensor-core path, at the image shape.

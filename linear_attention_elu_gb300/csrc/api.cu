@@ -289,6 +289,9 @@ la_status backward(bool causal, const void* q, const void* k, const void* v, con
     const size_t need = kHeaderBytes + body_bytes(op, B, H, N, Dk, Dv, dt);
     if ((s = check_workspace(workspace, workspace_bytes, need)) != LA_OK) return s;
     char* body = (char*)workspace + kHeaderBytes;
+    if (la::tc_bwd_supported(Dk, Dv, dt))
+        return from_cuda(la::tc_bwd(q, k, v, dout, dq, dk, dv, causal, BH, N, eps, phi, workspace,
+                                    body, (cudaStream_t)stream));
     return from_cuda(la::simt_bwd(q, k, v, dout, dq, dk, dv, dt, causal, BH, N, Dk, Dv, eps, phi,
                                   body, (cudaStream_t)stream));
 }

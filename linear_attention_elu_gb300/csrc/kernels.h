@@ -66,6 +66,21 @@ cudaError_t decode_step_strided(const void* q, const void* k, const void* v, voi
                                 float* z, la_dtype dt, int64_t BH, int D, int M, float eps, int fm,
                                 int H, int64_t ld_qk, int64_t ld_v, cudaStream_t st);
 
+// Scans of the tensor-core backward (csrc/simt.cu), in place over per-chunk
+// sums: the reverse exclusive sum (causal) or total (non-causal).
+cudaError_t bwd_reverse_sums(float* rstates, bool causal, int64_t BH, int nchunks, int E,
+                             cudaStream_t st);
+// The exclusive prefix (causal) or total (non-causal) of per-chunk states in place.
+cudaError_t bwd_prefix_states(float* states, bool causal, int64_t BH, int nchunks, int D, int M,
+                              cudaStream_t st);
+
+// Tensor-core backward (csrc/bwd_tc.cu): bf16, Dk = Dv = 64; same workspace as
+// the fp32 backward (simt_bwd_workspace).
+bool tc_bwd_supported(int D, int M, la_dtype dt);
+cudaError_t tc_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                   void* dk, void* dv, bool causal, int64_t BH, int N, float eps, int fm,
+                   void* ws_header, void* scratch, cudaStream_t st);
+
 // Layer decode step (csrc/layer.cu): workspace bytes after the header.
 size_t layer_workspace(int B, int H, int D, la_dtype dt);
 

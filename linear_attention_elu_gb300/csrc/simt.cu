@@ -1085,6 +1085,28 @@ cudaError_t simt_noncausal(const void* q, const void* k, const void* v, void* o,
                                               total, st);
 }
 
+cudaError_t bwd_prefix_states(float* states, bool causal, int64_t BH, int nchunks, int D, int M,
+                              cudaStream_t st) {
+    const int E = D * M + D;
+    const unsigned sgrid = (unsigned)((BH * (int64_t)E + 255) / 256);
+    if (causal)
+        chunk_scan_kernel<<<sgrid, 256, 0, st>>>(states, nullptr, nullptr, nullptr, nullptr, BH,
+                                                 nchunks, D, M);
+    else
+        chunk_total_kernel<<<sgrid, 256, 0, st>>>(states, BH, nchunks, E);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t bwd_reverse_sums(float* rstates, bool causal, int64_t BH, int nchunks, int E,
+                             cudaStream_t st) {
+    const unsigned sgrid = (unsigned)((BH * (int64_t)E + 255) / 256);
+    if (causal)
+        chunk_rscan_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
+    else
+        chunk_total_kernel<<<sgrid, 256, 0, st>>>(rstates, BH, nchunks, E);
+    return cudaPeekAtLastError();
+}
+
 size_t simt_bwd_workspace(int64_t BH, int N, int D, int M) {
     const int nchunks = (N + kChunk - 1) / kChunk;
     return sizeof(float) * ((size_t)2 * BH * nchunks * (size_t)(D * M + D) +

@@ -119,3 +119,39 @@ def test_wide_heads_are_refused(la):
         with pytest.raises(la.LinAttnError) as e:
             fn(q, k, v, torch.zeros_like(v))
         assert e.value.status == 2  # LA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,N", [(1, 1, 2), (1, 2, 127), (2, 1, 128), (1, 2, 129),
+                                   (2, 3, 1000), (8, 8, 3072)])
+def test_bf16_tensor_core_gradients(la, causal, B, H, N):
+    # bf16 with Dk = Dv = 64 runs on the tensor-core kernels (128-token chunks):
+    # two rows, exact chunk multiples, ragged tails and the image shape. (One
+    # token alone is ill-conditioned for this measure: its dq, dk are the
+    # cancellation residue g.(v - o) with o = v up to eps, so the head-wise scale
+    # is the residue itself; the first-row test covers it in absolute terms.)
+    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=N + 17 + causal)
+    g = make_qkv(B, H, N, 64, "bf16", seed=N + 18)[2]
+    dev = torch.device("cuda")
+    fn = la.la_causal_bwd if causal else la.la_noncausal_bwd
+    dq, dk, dv = fn(q.to(dev), k.to(dev), v.to(dev), g.to(dev))
+    torch.cuda.synchronize()
+    heads = slice(None) if B * H <= 6 else slice(0, 3)
+    qf, kf, vf, gf = (to_f64(t).reshape(B * H, N, 64)[heads] for t in (q, k, v, g))
+    rq, rk, rv = bwd.grads(qf, kf, vf, gf, causal)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = headwise_rel(to_f64(got).reshape(B * H, N, 64)[heads], ref)
+        assert err <= TOL["bf16"], (name, err)
+
+
+def test_bf16_causal_first_row_only_touches_first_token(la):
+    # The tensor-core path keeps causality exactly: a loss on row 0 of a head
+    # leaves every later token's gradients zero.
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 300, 64, "bf16", seed=5))
+    g = torch.zeros_like(v)
+    g[0, 0, 0] = torch.randn(64, device="cuda").bfloat16()
+    dq, dk, dv = la.la_causal_bwd(q, k, v, g)
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert float(t[0, 0, 1:].float().abs().max()) == 0
+    assert float(dv[0, 0, 0].float().abs().max()) > 0
