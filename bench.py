@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--workload", default="long", choices=["image", "long"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--also-only", default=None,
+                   help="comma-separated names of the secondary measurements to run")
     p.add_argument("--no-also", action="store_true",
                    help="skip the secondary non-causal and decode measurements")
     return p.parse_args()
@@ -351,299 +353,319 @@ def causal_also(la, w, dev, stream, calls=100):
             "status": la.la_query_status(ws)}
 
 
-def other_paths(la, dev, stream, main_workload):
-    """Secondary measurements: the other causal shape and the other operations of the path."""
+def other_paths(la, dev, stream, main_workload, only=None):
+    """Secondary measurements: the other causal shape and the other operations of
+    the path (`only`: the names of the entries to measure, all when None)."""
     hbm, _ = peaks()
     out = {}
-    other = "image" if main_workload == "long" else "long"
-    out[other] = causal_also(la, WORKLOADS[other], dev, stream, calls=200 if other == "image" else 20)
-    # Non-causal, B=16 H=8 N=8192 D=128 bf16 (one 1.07 GB input set, larger than L2).
-    w = WORKLOADS["bidir"]
+
+    def want(name):
+        return only is None or name in only
+
     gen = torch.Generator(device=dev)
     gen.manual_seed(123)
-    q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
-               for _ in range(3))
-    o = torch.empty_like(v)
-    ws = la.workspace(la.LA_OP_NONCAUSAL, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
-    for _ in range(3):
-        la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
-    g = torch.cuda.CUDAGraph()
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g):
-        la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
-    g.replay()
-    torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 10
-    a.record(stream)
-    for _ in range(reps):
-        g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
-    alg = w.tokens * 4 * w.D * 2
-    out["noncausal"] = {"workload": w.name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
-                        "ms_per_call": ms, "alg_GBps": alg / (ms * 1e-3) / 1e9,
-                        "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm,
-                        "status": la.la_query_status(ws)}
-    del q, k, v, o, ws, g
-    # Non-causal at D = 64 on the image shape (B=8 H=8 N=3072 bf16): 100.7 MB per call,
-    # six rotating input sets so that each use finds its inputs outside L2.
-    w = WORKLOADS["image"]
-    sets = []
-    for r in range(6):
+    us = None                               # decode step time, for the layer entry
+    other = "image" if main_workload == "long" else "long"
+    if want(other):
+        out[other] = causal_also(la, WORKLOADS[other], dev, stream,
+                                 calls=200 if other == "image" else 20)
+    if want("noncausal"):
+        # Non-causal, B=16 H=8 N=8192 D=128 bf16 (one 1.07 GB input set, larger than L2).
+        w = WORKLOADS["bidir"]
         q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
                    for _ in range(3))
-        sets.append((q, k, v, torch.empty_like(v)))
-    ws = la.workspace(la.LA_OP_NONCAUSAL, w.B, w.H, w.N, w.D, w.D, torch.bfloat16, dev)
-    for i in range(6):
-        q, k, v, o = sets[i]
-        la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    reps = 60
-    with torch.cuda.graph(g):
-        for i in range(reps):
-            q, k, v, o = sets[i % 6]
-            la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
-    g.replay()
-    torch.cuda.synchronize()
-    a.record(stream)
-    g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
-    alg = w.tokens * 4 * w.D * 2
-    out["noncausal_d64"] = {"workload": w.name.replace("causal", "non-causal"),
-                            "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
-                            "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
-                                         "peak": hbm, "unit": "GB/s",
-                                         "frac": alg / (ms * 1e-3) / 1e9 / hbm},
-                            "status": la.la_query_status(ws)}
-    del sets, ws, g
-    # L2 reference for the decode step, whose fp32 state stays in L2 between steps:
-    # an in-place scale of a 64 MB fp32 buffer (each byte read and written at the
-    # same address, as the decode step does with S and z), 200 launches in one graph.
-    x = torch.ones(16 * 2 ** 20, device=dev)
-    g = torch.cuda.CUDAGraph()
-    x.mul_(1.0)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g):
-        for _ in range(200):
-            x.mul_(1.0)
-    best = None
-    for _ in range(3):
-        g.replay()
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        t = a.elapsed_time(b) / 200
-        best = t if best is None else min(best, t)
-    l2_gbps = 2 * x.numel() * 4 / (best * 1e-3) / 1e9
-    out["l2_peak"] = {"GBps": l2_gbps, "how": "torch in-place x.mul_(1.0) over a 64 MB fp32 "
-                      "buffer (read + write, L2-resident), 200 launches in one CUDA graph, best of 3"}
-    del x, g
-
-    def decode_run(B, T):
-        """us per step of T consecutive decode steps in one graph (B sequences x 8 heads)."""
-        w = WORKLOADS["decode"]
-        q, k, v = (torch.randn(T, B, w.H, w.D, device=dev, generator=gen).bfloat16()
-                   for _ in range(3))
         o = torch.empty_like(v)
-        S = torch.zeros(B, w.H, w.D, w.D, device=dev)
-        z = torch.zeros(B, w.H, w.D, device=dev)
-
-        def steps():
-            for t in range(T):
-                la.la_decode_step(q[t], k[t], v[t], S, z, o=o[t])
-
-        steps()
+        ws = la.workspace(la.LA_OP_NONCAUSAL, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
+        for _ in range(3):
+            la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        alg = w.tokens * 4 * w.D * 2
+        out["noncausal"] = {"workload": w.name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+                            "ms_per_call": ms, "alg_GBps": alg / (ms * 1e-3) / 1e9,
+                            "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm,
+                            "status": la.la_query_status(ws)}
+        del q, k, v, o, ws, g
+    if want("noncausal_d64"):
+        # Non-causal at D = 64 on the image shape (B=8 H=8 N=3072 bf16): 100.7 MB per call,
+        # six rotating input sets so that each use finds its inputs outside L2.
+        w = WORKLOADS["image"]
+        sets = []
+        for r in range(6):
+            q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
+                       for _ in range(3))
+            sets.append((q, k, v, torch.empty_like(v)))
+        ws = la.workspace(la.LA_OP_NONCAUSAL, w.B, w.H, w.N, w.D, w.D, torch.bfloat16, dev)
+        for i in range(6):
+            q, k, v, o = sets[i]
+            la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
+        reps = 60
         with torch.cuda.graph(g):
+            for i in range(reps):
+                q, k, v, o = sets[i % 6]
+                la.la_noncausal_fwd(q, k, v, o=o, ws=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        alg = w.tokens * 4 * w.D * 2
+        out["noncausal_d64"] = {"workload": w.name.replace("causal", "non-causal"),
+                                "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+                                "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
+                                             "peak": hbm, "unit": "GB/s",
+                                             "frac": alg / (ms * 1e-3) / 1e9 / hbm},
+                                "status": la.la_query_status(ws)}
+        del sets, ws, g
+    if want("decode") or want("decode_2048") or want("l2_peak"):
+        # L2 reference for the decode step, whose fp32 state stays in L2 between steps:
+        # an in-place scale of a 64 MB fp32 buffer (each byte read and written at the
+        # same address, as the decode step does with S and z), 200 launches in one graph.
+        x = torch.ones(16 * 2 ** 20, device=dev)
+        g = torch.cuda.CUDAGraph()
+        x.mul_(1.0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for _ in range(200):
+                x.mul_(1.0)
+        best = None
+        for _ in range(3):
+            g.replay()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b) / 200
+            best = t if best is None else min(best, t)
+        l2_gbps = 2 * x.numel() * 4 / (best * 1e-3) / 1e9
+        out["l2_peak"] = {"GBps": l2_gbps, "how": "torch in-place x.mul_(1.0) over a 64 MB fp32 "
+                          "buffer (read + write, L2-resident), 200 launches in one CUDA graph, best of 3"}
+        del x, g
+
+        def decode_run(B, T):
+            """us per step of T consecutive decode steps in one graph (B sequences x 8 heads)."""
+            w = WORKLOADS["decode"]
+            q, k, v = (torch.randn(T, B, w.H, w.D, device=dev, generator=gen).bfloat16()
+                       for _ in range(3))
+            o = torch.empty_like(v)
+            S = torch.zeros(B, w.H, w.D, w.D, device=dev)
+            z = torch.zeros(B, w.H, w.D, device=dev)
+
+            def steps():
+                for t in range(T):
+                    la.la_decode_step(q[t], k[t], v[t], S, z, o=o[t])
+
             steps()
-        g.replay()
-        torch.cuda.synchronize()
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / T * 1e3
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                steps()
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / T * 1e3
 
-    # Decode, 512 sequences x 8 heads, D=64: all 3072 steps of the configuration in one
-    # graph. The 68 MB fp32 state stays in the 129 MB L2 between steps, so its
-    # roofline is the L2 read+write rate above.
-    w = WORKLOADS["decode"]
-    us = decode_run(w.B, w.N)
-    per_step = 33792 * w.B * w.H
-    gbps = per_step / (us * 1e-6) / 1e9
-    out["decode"] = {"workload": w.name + ", all steps timed", "value": 1e6 / us,
-                     "unit": "steps/s", "us_per_step": us, "alg_GBps": gbps,
-                     "roofline": {"bound": "l2", "achieved": gbps, "peak": l2_gbps,
-                                  "unit": "GB/s", "frac": gbps / l2_gbps,
-                                  "peak_source": "l2_peak (measured in this run)"},
-                     "frac_of_hbm": gbps / hbm,
-                     "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
-    # The same step with 2048 sequences x 8 heads: 272 MB of fp32 state, larger than
-    # L2, so every step streams it from and to HBM.
-    Bbig, Tbig = 2048, 256
-    us_big = decode_run(Bbig, Tbig)
-    per_big = 33792 * Bbig * w.H
-    gbps_big = per_big / (us_big * 1e-6) / 1e9
-    out["decode_2048"] = {"workload": f"decode {Bbig} seq x H=8 D=64 bf16, fp32 state 272 MB, "
-                                      f"{Tbig} steps timed",
-                          "value": 1e6 / us_big, "unit": "steps/s", "us_per_step": us_big,
-                          "alg_GBps": gbps_big,
-                          "roofline": {"bound": "hbm", "achieved": gbps_big, "peak": hbm,
-                                       "unit": "GB/s", "frac": gbps_big / hbm}}
-    T = 256
-    # Layer decode step at the same batch (512 sequences, d_model = 8 x 64, bf16,
-    # synthetic weights): QKV projection, the decode step, output projection.
-    dm = w.H * w.D
-    Wqkv = (torch.randn(dm, 3 * dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
-    Wo = (torch.randn(dm, dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
-    xs = torch.randn(T, w.B, dm, device=dev, generator=gen).bfloat16()
-    ys = torch.empty_like(xs)
-    S = torch.zeros(w.B, w.H, w.D, w.D, device=dev)
-    z = torch.zeros(w.B, w.H, w.D, device=dev)
-    ws = la.workspace(la.LA_OP_LAYER_DECODE, w.B, w.H, 1, w.D, w.D, xs.dtype, dev)
+        # Decode, 512 sequences x 8 heads, D=64: all 3072 steps of the configuration in one
+        # graph. The 68 MB fp32 state stays in the 129 MB L2 between steps, so its
+        # roofline is the L2 read+write rate above.
+        w = WORKLOADS["decode"]
+        us = decode_run(w.B, w.N)
+        per_step = 33792 * w.B * w.H
+        gbps = per_step / (us * 1e-6) / 1e9
+        out["decode"] = {"workload": w.name + ", all steps timed", "value": 1e6 / us,
+                         "unit": "steps/s", "us_per_step": us, "alg_GBps": gbps,
+                         "roofline": {"bound": "l2", "achieved": gbps, "peak": l2_gbps,
+                                      "unit": "GB/s", "frac": gbps / l2_gbps,
+                                      "peak_source": "l2_peak (measured in this run)"},
+                         "frac_of_hbm": gbps / hbm,
+                         "note": "the 68 MB fp32 state stays resident in the 129 MB L2 across steps"}
+        # The same step with 2048 sequences x 8 heads: 272 MB of fp32 state, larger than
+        # L2, so every step streams it from and to HBM.
+        Bbig, Tbig = 2048, 256
+        us_big = decode_run(Bbig, Tbig)
+        per_big = 33792 * Bbig * w.H
+        gbps_big = per_big / (us_big * 1e-6) / 1e9
+        out["decode_2048"] = {"workload": f"decode {Bbig} seq x H=8 D=64 bf16, fp32 state 272 MB, "
+                                          f"{Tbig} steps timed",
+                              "value": 1e6 / us_big, "unit": "steps/s", "us_per_step": us_big,
+                              "alg_GBps": gbps_big,
+                              "roofline": {"bound": "hbm", "achieved": gbps_big, "peak": hbm,
+                                           "unit": "GB/s", "frac": gbps_big / hbm}}
+    if want("layer_decode"):
+        # Layer decode step at the same batch (512 sequences, d_model = 8 x 64, bf16,
+        # synthetic weights): QKV projection, the decode step, output projection.
+        w = WORKLOADS["decode"]
+        T = 256
+        dm = w.H * w.D
+        Wqkv = (torch.randn(dm, 3 * dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
+        Wo = (torch.randn(dm, dm, device=dev, generator=gen) * dm ** -0.5).bfloat16()
+        xs = torch.randn(T, w.B, dm, device=dev, generator=gen).bfloat16()
+        ys = torch.empty_like(xs)
+        S = torch.zeros(w.B, w.H, w.D, w.D, device=dev)
+        z = torch.zeros(w.B, w.H, w.D, device=dev)
+        ws = la.workspace(la.LA_OP_LAYER_DECODE, w.B, w.H, 1, w.D, w.D, xs.dtype, dev)
 
-    def layer_steps():
-        for t in range(T):
-            la.la_layer_decode_step(xs[t], Wqkv, Wo, S, z, w.H, y=ys[t], ws=ws)
+        def layer_steps():
+            for t in range(T):
+                la.la_layer_decode_step(xs[t], Wqkv, Wo, S, z, w.H, y=ys[t], ws=ws)
 
-    layer_steps()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
         layer_steps()
-    g.replay()
-    torch.cuda.synchronize()
-    a.record(stream)
-    g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    lus = a.elapsed_time(b) / T * 1e3
-    gemm_flops = 2 * w.B * dm * 4 * dm
-    out["layer_decode"] = {
-        "workload": f"layer decode step, {w.B} sequences, d_model {dm} = {w.H} x {w.D}, bf16, "
-                    f"synthetic weights, {T} steps timed",
-        "value": 1e6 / lus, "unit": "steps/s", "us_per_step": lus,
-        "attention_share_est": us / lus,
-        "projection_tflops_if_rest": gemm_flops / max(lus - us, 1e-3) / 1e6,
-        "note": "projections: the library's tcgen05 bf16 products (128 x 64 tiles); "
-                "the decode step between them is the library's decode kernel"}
-    del Wqkv, Wo, xs, ys, S, z, ws, g
-    # Causal and non-causal forward on fp32 inputs (the fp32 SIMT path) at the
-    # image shape B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
-    w = WORKLOADS["image"]
-    q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen) for _ in range(3))
-    o = torch.empty_like(v)
-    for key, fn, op, macs, name in (
-            ("causal_f32", la.la_causal_fwd, la.LA_OP_CAUSAL, FWD_F32_MACS_PER_TOKEN_D64,
-             w.name.replace("bf16", "f32")),
-            ("noncausal_f32", la.la_noncausal_fwd, la.LA_OP_NONCAUSAL, NC_F32_MACS_PER_TOKEN_D64,
-             w.name.replace("bf16", "f32").replace("causal", "non-causal"))):
-        ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
-        fn(q, k, v, o=o, ws=ws)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            layer_steps()
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        lus = a.elapsed_time(b) / T * 1e3
+        gemm_flops = 2 * w.B * dm * 4 * dm
+        out["layer_decode"] = {
+            "workload": f"layer decode step, {w.B} sequences, d_model {dm} = {w.H} x {w.D}, bf16, "
+                        f"synthetic weights, {T} steps timed",
+            "value": 1e6 / lus, "unit": "steps/s", "us_per_step": lus,
+            "attention_share_est": us / lus if us else None,
+            "projection_tflops_if_rest": gemm_flops / max(lus - us, 1e-3) / 1e6 if us else None,
+            "note": "projections: the library's tcgen05 bf16 products (128 x 64 tiles); "
+                    "the decode step between them is the library's decode kernel"}
+        del Wqkv, Wo, xs, ys, S, z, ws, g
+    if want("causal_f32") or want("noncausal_f32"):
+        # Causal and non-causal forward on fp32 inputs (the fp32 SIMT path) at the
+        # image shape B=8 H=8 N=3072 D=64; 151 MB of inputs, larger than L2.
+        w = WORKLOADS["image"]
+        q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen) for _ in range(3))
+        o = torch.empty_like(v)
+        for key, fn, op, macs, name in (
+                ("causal_f32", la.la_causal_fwd, la.LA_OP_CAUSAL, FWD_F32_MACS_PER_TOKEN_D64,
+                 w.name.replace("bf16", "f32")),
+                ("noncausal_f32", la.la_noncausal_fwd, la.LA_OP_NONCAUSAL, NC_F32_MACS_PER_TOKEN_D64,
+                 w.name.replace("bf16", "f32").replace("causal", "non-causal"))):
+            ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
             fn(q, k, v, o=o, ws=ws)
-        g.replay()
-        torch.cuda.synchronize()
-        reps = 10
-        a.record(stream)
-        for _ in range(reps):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(q, k, v, o=o, ws=ws)
             g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        flops = w.tokens * 2 * macs
-        out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
-                    "ms_per_call": ms, "tflops": flops / (ms * 1e-3) / 1e12,
-                    "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
-                    "bound": "alu (fp32 FMA)"}
-        del ws, g
-    del q, k, v, o
-    # Causal and non-causal backward (tensor-core kernels for bf16 D = 64) at the
-    # image shape B=8 H=8 N=3072 D=64 bf16.
-    q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
-                     for _ in range(4))
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for key, fn, op, macs, name in (
-            ("causal_bwd", la.la_causal_bwd, la.LA_OP_CAUSAL_BWD, TC_BWD_MACS_PER_TOKEN_D64,
-             w.name.replace("causal", "causal backward")),
-            ("noncausal_bwd", la.la_noncausal_bwd, la.LA_OP_NONCAUSAL_BWD,
-             TC_NC_BWD_MACS_PER_TOKEN_D64, w.name.replace("causal", "non-causal backward"))):
-        ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
-        fn(q, k, v, dout, dq, dk, dv, ws=ws)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+            torch.cuda.synchronize()
+            reps = 10
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            flops = w.tokens * 2 * macs
+            out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+                        "ms_per_call": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                        "frac_of_fp32_fma": flops / (ms * 1e-3) / FP32_FMA_PEAK,
+                        "bound": "alu (fp32 FMA)"}
+            del ws, g
+        del q, k, v, o
+    if want("causal_bwd") or want("noncausal_bwd"):
+        # Causal and non-causal backward (tensor-core kernels for bf16 D = 64) at the
+        # image shape B=8 H=8 N=3072 D=64 bf16.
+        w = WORKLOADS["image"]
+        q, k, v, dout = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
+                         for _ in range(4))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for key, fn, op, macs, name in (
+                ("causal_bwd", la.la_causal_bwd, la.LA_OP_CAUSAL_BWD, TC_BWD_MACS_PER_TOKEN_D64,
+                 w.name.replace("causal", "causal backward")),
+                ("noncausal_bwd", la.la_noncausal_bwd, la.LA_OP_NONCAUSAL_BWD,
+                 TC_NC_BWD_MACS_PER_TOKEN_D64, w.name.replace("causal", "non-causal backward"))):
+            ws = la.workspace(op, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
             fn(q, k, v, dout, dq, dk, dv, ws=ws)
-        g.replay()
-        torch.cuda.synchronize()
-        reps = 5
-        a.record(stream)
-        for _ in range(reps):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(q, k, v, dout, dq, dk, dv, ws=ws)
             g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        flops = w.tokens * 2 * macs
-        gbps = w.tokens * BWD_ALG_BYTES_PER_TOKEN_D64 / (ms * 1e-3) / 1e9
-        out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
-                    "ms_per_call": ms, "tflops_executed": flops / (ms * 1e-3) / 1e12,
-                    "frac_of_bf16_dense": flops / (ms * 1e-3) / 1e12 / bf16_peak(),
-                    "alg_GBps": gbps, "frac_of_hbm": gbps / hbm,
-                    "bound": "latency: one CTA per 128-token chunk runs load, MMAs and "
-                             "epilogue in sequence (neither pipe nor DRAM saturated)"}
-        del ws, g
-    # Positive random features (R = 64, x scaled by D^-1/4) of q and k, then the
-    # identity-map causal forward on the tensor-core path, at the image shape.
-    R = 64
-    W = torch.randn(R, w.D, device=dev, generator=gen).bfloat16()
-    qs, ks = (q.float() * w.D ** -0.25).bfloat16(), (k.float() * w.D ** -0.25).bfloat16()
-    fq = torch.empty(w.B, w.H, w.N, R, device=dev, dtype=torch.bfloat16)
-    fk = torch.empty_like(fq)
-    o = torch.empty_like(v)
-    ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, R, w.D, q.dtype, dev)
+            torch.cuda.synchronize()
+            reps = 5
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            flops = w.tokens * 2 * macs
+            gbps = w.tokens * BWD_ALG_BYTES_PER_TOKEN_D64 / (ms * 1e-3) / 1e9
+            out[key] = {"workload": name, "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+                        "ms_per_call": ms, "tflops_executed": flops / (ms * 1e-3) / 1e12,
+                        "frac_of_bf16_dense": flops / (ms * 1e-3) / 1e12 / bf16_peak(),
+                        "alg_GBps": gbps, "frac_of_hbm": gbps / hbm,
+                        "bound": "latency: one CTA per 128-token chunk runs load, MMAs and "
+                                 "epilogue in sequence (neither pipe nor DRAM saturated)"}
+            del ws, g
+    if want("random_features_causal"):
+        # Positive random features (R = 64, x scaled by D^-1/4) of q and k, then the
+        # identity-map causal forward on the tensor-core path, at the image shape.
+        w = WORKLOADS["image"]
+        q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
+                   for _ in range(3))
+        R = 64
+        W = torch.randn(R, w.D, device=dev, generator=gen).bfloat16()
+        qs, ks = (q.float() * w.D ** -0.25).bfloat16(), (k.float() * w.D ** -0.25).bfloat16()
+        fq = torch.empty(w.B, w.H, w.N, R, device=dev, dtype=torch.bfloat16)
+        fk = torch.empty_like(fq)
+        o = torch.empty_like(v)
+        ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, R, w.D, q.dtype, dev)
 
-    def features():
-        la.la_positive_random_features(qs, W, out=fq)
-        la.la_positive_random_features(ks, W, out=fk)
+        def features():
+            la.la_positive_random_features(qs, W, out=fq)
+            la.la_positive_random_features(ks, W, out=fk)
 
-    def chain():
-        features()
-        la.la_causal_fwd(fq, fk, v, o=o, ws=ws, phi=la.LA_PHI_IDENTITY)
+        def chain():
+            features()
+            la.la_causal_fwd(fq, fk, v, o=o, ws=ws, phi=la.LA_PHI_IDENTITY)
 
-    res = {}
-    for name, fn in (("features_ms", features), ("chain_ms", chain)):
-        fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        res = {}
+        for name, fn in (("features_ms", features), ("chain_ms", chain)):
             fn()
-        g.replay()
-        torch.cuda.synchronize()
-        reps = 10
-        a.record(stream)
-        for _ in range(reps):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
             g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        res[name] = a.elapsed_time(b) / reps
-        del g
-    rows = 2 * w.tokens
-    feat_bytes = rows * (w.D + R) * 2          # x read and features written once, bf16
-    out["random_features_causal"] = {
-        "workload": w.name.replace("causal", "random features (R=64) + identity-map causal"),
-        "value": w.tokens / (res["chain_ms"] * 1e-3), "unit": "tokens/s", **res,
-        "features_alg_GBps": feat_bytes / (res["features_ms"] * 1e-3) / 1e9,
-        "features_frac_of_hbm": feat_bytes / (res["features_ms"] * 1e-3) / 1e9 / hbm,
-        "bound": "features: hbm (tcgen05 projection, exp epilogue); attention: as the causal path"}
+            torch.cuda.synchronize()
+            reps = 10
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) / reps
+            del g
+        rows = 2 * w.tokens
+        feat_bytes = rows * (w.D + R) * 2          # x read and features written once, bf16
+        out["random_features_causal"] = {
+            "workload": w.name.replace("causal", "random features (R=64) + identity-map causal"),
+            "value": w.tokens / (res["chain_ms"] * 1e-3), "unit": "tokens/s", **res,
+            "features_alg_GBps": feat_bytes / (res["features_ms"] * 1e-3) / 1e9,
+            "features_frac_of_hbm": feat_bytes / (res["features_ms"] * 1e-3) / 1e9 / hbm,
+            "bound": "features: hbm (tcgen05 projection, exp epilogue); attention: as the causal path"}
     return out
 
 
@@ -778,7 +800,8 @@ def main():
     d2h = ho.numel() * ho.element_size()
     del sets, graphs, g_warm, g_timed
 
-    also = {} if args.no_also else other_paths(la, dev, stream, args.workload)
+    only = set(args.also_only.split(",")) if args.also_only else None
+    also = {} if args.no_also else other_paths(la, dev, stream, args.workload, only)
 
     hbm, src = peaks()
     # Average launch duration over the timed region (events around the K steps);

@@ -155,9 +155,20 @@ __device__ __forceinline__ void state_rows_to_tile(uint8_t* dst, const float* sr
                                                    int t) {
     const int r = t & 63, p = t >> 6;
     float f[16];
+    if (transposed) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-        f[e] = transposed ? src[(16 * p + e) * kD + r] : src[r * kD + 16 * p + e];
+        for (int e = 0; e < 16; ++e) f[e] = src[(16 * p + e) * kD + r];
+    } else {
+        // 16 consecutive floats: four 16-byte loads (the block is 16-byte aligned).
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 x = reinterpret_cast<const float4*>(src + r * kD + 16 * p)[e4];
+            f[4 * e4] = x.x;
+            f[4 * e4 + 1] = x.y;
+            f[4 * e4 + 2] = x.z;
+            f[4 * e4 + 3] = x.w;
+        }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
         *reinterpret_cast<uint4*>(dst + sw128_offset(r, 16 * p + 8 * h)) =
