@@ -398,6 +398,39 @@ def other_paths(la, dev, stream, main_workload, only=None):
                             "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm,
                             "status": la.la_query_status(ws)}
         del q, k, v, o, ws, g
+    if want("causal_d128"):
+        # Causal at D = 128 on the bidirectional workload's shape (B=16 H=8 N=8192 bf16):
+        # run sums, seed scan and output pass; one 1.07 GB input set, larger than L2.
+        w = WORKLOADS["bidir"]
+        q, k, v = (torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=gen).bfloat16()
+                   for _ in range(3))
+        o = torch.empty_like(v)
+        ws = la.workspace(la.LA_OP_CAUSAL, w.B, w.H, w.N, w.D, w.D, q.dtype, dev)
+        for _ in range(3):
+            la.la_causal_fwd(q, k, v, o=o, ws=ws)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            la.la_causal_fwd(q, k, v, o=o, ws=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = 10
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        alg = w.tokens * 4 * w.D * 2
+        out["causal_d128"] = {"workload": w.name.replace("non-causal", "causal"),
+                              "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms,
+                              "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9,
+                                           "peak": hbm, "unit": "GB/s",
+                                           "frac": alg / (ms * 1e-3) / 1e9 / hbm},
+                              "launches_per_call": la.la_launch_count(la.LA_OP_CAUSAL, w.B, w.H, w.N,
+                                                                      w.D, w.D, la.LA_BF16),
+                              "status": la.la_query_status(ws)}
+        del q, k, v, o, ws, g
     if want("noncausal_d64"):
         # Non-causal at D = 64 on the image shape (B=8 H=8 N=3072 bf16): 100.7 MB per call,
         # six rotating input sets so that each use finds its inputs outside L2.

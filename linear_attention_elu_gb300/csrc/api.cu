@@ -42,7 +42,7 @@ size_t body_bytes(la_op op, int B, int H, int N, int Dk, int Dv, la_dtype dt) {
     if (BH == 0 || N == 0) return 0;
     switch (op) {
         case LA_OP_CAUSAL:
-            if (la::tc_causal_supported(Dk, Dv, dt)) return la::tc_causal_workspace(BH, N);
+            if (la::tc_causal_supported(Dk, Dv, dt)) return la::tc_causal_workspace(BH, N, Dk);
             return la::simt_causal_workspace(BH, N, Dk, Dv);
         case LA_OP_NONCAUSAL:
             if (la::tc_noncausal_supported(Dk, Dv, dt)) return la::tc_noncausal_workspace(BH, N, Dk);
@@ -122,7 +122,7 @@ la_status causal_fwd(const void* q, const void* k, const void* v, void* o, int B
     char* body = (char*)workspace + kHeaderBytes;
     if (la::tc_causal_supported(Dk, Dv, dt))
         return from_cuda(
-            la::tc_causal(q, k, v, o, BH, N, eps, phi, S0, z0, S_out, z_out, workspace, body, st));
+            la::tc_causal(q, k, v, o, BH, N, Dk, eps, phi, S0, z0, S_out, z_out, workspace, body, st));
     return from_cuda(la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, phi, S0, z0, S_out, z_out,
                                      body, st));
 }
@@ -191,7 +191,7 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
     else if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD)
         *launches = 5;
     else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
-        *launches = la::tc_causal_launches();
+        *launches = la::tc_causal_launches(Dk);
     else if (op == LA_OP_NONCAUSAL && la::tc_noncausal_supported(Dk, Dv, dt))
         *launches = 2;
     else

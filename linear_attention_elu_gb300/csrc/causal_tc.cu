@@ -810,20 +810,25 @@ int grid_cap() { return sm_count(); }
 
 }  // namespace
 
-bool tc_causal_supported(int D, int M, la_dtype dt) { return dt == LA_BF16 && D == 64 && M == 64; }
+bool tc_causal_supported(int D, int M, la_dtype dt) {
+    return dt == LA_BF16 && D == M && (D == 64 || D == 128);
+}
 
-// Workspace after the header: per CTA one published sum and one inclusive prefix
-// (tagged 64-bit words).
-size_t tc_causal_workspace(int64_t BH, int N) {
+// Workspace after the header. D = 64: per CTA one published sum and one
+// inclusive prefix (tagged 64-bit words). D = 128: the run sums and seeds.
+size_t tc_causal_workspace(int64_t BH, int N, int D) {
+    if (D == 128) return tc_causal128_workspace(BH, N);
     Partition p = make_partition(BH, N, grid_cap());
     return 2 * sizeof(uint64_t) * (size_t)p.grid * kE;
 }
 
-int tc_causal_launches() { return 1; }
+int tc_causal_launches(int D) { return D == 128 ? 3 : 1; }
 
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, int fm, const float* S0, const float* z0, float* S_out,
+                      int D, float eps, int fm, const float* S0, const float* z0, float* S_out,
                       float* z_out, void* ws_header, void* scratch, cudaStream_t st) {
+    if (D == 128)
+        return tc_causal128(q, k, v, o, BH, N, eps, fm, S0, z0, S_out, z_out, ws_header, scratch, st);
     Partition p = make_partition(BH, N, grid_cap());
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     uint64_t* agg = reinterpret_cast<uint64_t*>(scratch);

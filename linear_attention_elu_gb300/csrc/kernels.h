@@ -42,15 +42,20 @@ bool tc_random_features_supported(int D, int R, la_dtype dt);
 cudaError_t tc_random_features(const void* x, const void* W, void* out, int64_t rows, float shift,
                                cudaStream_t st);
 
-// Tensor-core (tcgen05) causal path: bf16, Dk = Dv = 64.
+// Tensor-core (tcgen05) causal path: bf16, Dk = Dv = 64 (one fused launch,
+// causal_tc.cu) or 128 (run sums, seed scan, output pass: causal128_tc.cu).
 bool tc_causal_supported(int D, int M, la_dtype dt);
-size_t tc_causal_workspace(int64_t BH, int N);
-int tc_causal_launches();
+size_t tc_causal_workspace(int64_t BH, int N, int D);
+int tc_causal_launches(int D);
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
-                      float eps, int fm, const float* S0, const float* z0, float* S_out,
+                      int D, float eps, int fm, const float* S0, const float* z0, float* S_out,
                       float* z_out, void* ws_header, void* scratch, cudaStream_t st);
+size_t tc_causal128_workspace(int64_t BH, int N);
+cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
+                         float eps, int fm, const float* S0, const float* z0, float* S_out,
+                         float* z_out, void* ws_header, void* scratch, cudaStream_t st);
 
-// Tensor-core (tcgen05) non-causal path: bf16, Dk = Dv = 128.
+// Tensor-core (tcgen05) non-causal path: bf16, Dk = Dv = 64 or 128.
 bool tc_noncausal_supported(int D, int M, la_dtype dt);
 size_t tc_noncausal_workspace(int64_t BH, int N, int D);
 cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,

@@ -107,10 +107,17 @@ extern "C" la_status la_causal_fwd_noalloc(const void* q, const void* k, const v
     if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return LA_ERR_INVALID_ARG;
     if ((S_out && !aligned16(S_out)) || (z_out && !aligned16(z_out))) return LA_ERR_INVALID_ARG;
-    const bool tc = la::tc_causal_supported(Dk, Dv, dt);
-    const size_t body = tc ? la::tc_causal_workspace(BH, N)
-                           : la::simt_causal_workspace(BH, N, Dk, Dv);
+    // Tensor-core path when its workspace fits the array; at Dk = Dv = 128 its run
+    // sums outgrow the array before the fp32 path's chunk states do on short
+    // sequences, so the fp32 path takes what the tensor-core path cannot.
+    bool tc = la::tc_causal_supported(Dk, Dv, dt);
+    size_t body = tc ? la::tc_causal_workspace(BH, N, Dk) : la::simt_causal_workspace(BH, N, Dk, Dv);
+    if (tc && Dk != 64 && kHeaderBytes + body > kNoAllocScratchBytes) {
+        tc = false;
+        body = la::simt_causal_workspace(BH, N, Dk, Dv);
+    }
     if (kHeaderBytes + body > kNoAllocScratchBytes) return LA_ERR_WORKSPACE;  // beyond capacity
+    const bool tagged = tc && Dk == 64;   // the only path that reads tagged words
     cudaStream_t st = (cudaStream_t)stream;
     int dev = -1;
     la_status s = current_device(&dev);
@@ -121,14 +128,14 @@ extern "C" la_status la_causal_fwd_noalloc(const void* q, const void* k, const v
     char* scratch = static_cast<char*>(ws) + kHeaderBytes;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (tc && g_body_untagged[dev]) {
+        if (tagged && g_body_untagged[dev]) {
             if (cudaMemsetAsync(scratch, 0, body, st) != cudaSuccess) return LA_ERR_CUDA;
             g_body_untagged[dev] = false;
         }
-        if (!tc) g_body_untagged[dev] = true;
+        if (!tagged) g_body_untagged[dev] = true;
     }
-    cudaError_t err = tc ? la::tc_causal(q, k, v, o, BH, N, eps, LA_PHI_ELU1, nullptr, nullptr, S_out,
-                                         z_out, ws, scratch, st)
+    cudaError_t err = tc ? la::tc_causal(q, k, v, o, BH, N, Dk, eps, LA_PHI_ELU1, nullptr, nullptr,
+                                         S_out, z_out, ws, scratch, st)
                          : la::simt_causal(q, k, v, o, dt, BH, N, Dk, Dv, eps, LA_PHI_ELU1, nullptr,
                                            nullptr, S_out, z_out, scratch, st);
     return err == cudaSuccess ? LA_OK : LA_ERR_CUDA;

@@ -640,6 +640,17 @@ cudaError_t launch_noncausal(const CUtensorMap& qm, const CUtensorMap& km, const
 
 }  // namespace
 
+cudaError_t tc_run_sums128(const CUtensorMap& kmap, const CUtensorMap& vmap, float* agg,
+                           const Partition& p, int N, int fm, WsHeader* hdr, cudaStream_t st) {
+    const bool ident = fm == kPhiIdentity;
+    auto state_kernel = ident ? nc_state_kernel<128, kPhiIdentity> : nc_state_kernel<128, kPhiElu1>;
+    static std::atomic<int> optin[2][kMaxDevices];
+    cudaError_t err = ensure_smem_optin(state_kernel, (int)kSSmem<128>, optin[ident]);
+    if (err) return err;
+    state_kernel<<<p.grid, kSThreads, kSSmem<128>, st>>>(kmap, vmap, agg, p, N, hdr);
+    return cudaPeekAtLastError();
+}
+
 cudaError_t tc_noncausal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                          int D, float eps, int fm, void* ws_header, void* scratch, cudaStream_t st) {
     Partition p = make_partition(BH, N, sm_count());

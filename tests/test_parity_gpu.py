@@ -249,23 +249,25 @@ def test_decode_sequence_equals_causal(la):
 # ------------------------------------------------------------ tensor-core causal path
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 1, 128), (1, 1, 129), (2, 3, 1000),
                                    (1, 2, 20000), (3, 5, 777), (40, 8, 256), (1, 1, 4096)])
-def test_tc_causal_partitions(la, B, H, N):
+def test_tc_causal_partitions(la, B, H, N, D):
     # Grids smaller than the SM count, heads spread over many CTAs, ragged tails.
-    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=B * 100 + H * 10 + N)
+    q, k, v = make_qkv(B, H, N, D, "bf16", seed=B * 100 + H * 10 + N + (D - 64))
     err = rowwise_rel(run(la, "causal", q, k, v), ref("causal", q, k, v))
     assert err <= TOL["bf16"], err
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("B,H,N", [(2, 3, 1500), (4, 64, 200), (8, 64, 100)])
-def test_tc_causal_final_state(la, B, H, N):
+def test_tc_causal_final_state(la, B, H, N, D):
     # (4, 64, 200) and (8, 64, 100): ranges of three or more chunks hold several
     # head ends, so one CTA writes several final states.
-    q, k, v = make_qkv(B, H, N, 64, "bf16", seed=21 + N)
+    q, k, v = make_qkv(B, H, N, D, "bf16", seed=21 + N + D)
     dev = torch.device("cuda")
-    S = torch.full((B, H, 64, 64), float("nan"), device=dev)
-    z = torch.full((B, H, 64), float("nan"), device=dev)
+    S = torch.full((B, H, D, D), float("nan"), device=dev)
+    z = torch.full((B, H, D), float("nan"), device=dev)
     la.la_causal_fwd(q.to(dev), k.to(dev), v.to(dev), S_out=S, z_out=z)
     torch.cuda.synchronize()
     _, Sr, zr = oracle.recurrent(to_f64(q), to_f64(k), to_f64(v), True, return_state=True)

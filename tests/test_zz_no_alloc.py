@@ -9,7 +9,9 @@ into a new result. They also run the fp32 path at the array's exact capacity,
 alternate fp32 and bf16 calls (the fp32 path leaves per-chunk fp32 states
 where the bf16 path reads tagged words), make a bounded wait run out through
 the header's test hook and read the status back, and check that host memory
-is refused before any launch. This file is collected last on purpose.
+is refused before any launch, and take the 128-wide bf16 path both where its
+run sums fit the array and where the fp32 path must take the call instead.
+This file is collected last on purpose.
 """
 import ctypes
 
@@ -54,13 +56,13 @@ def _call(so, q, k, v, o, S, z, dtype):
                                     torch.cuda.current_stream().cuda_stream)
 
 
-def _check_against_oracle(la, so, B, H, N, dtype, seed, with_workspace_entry=True):
+def _check_against_oracle(la, so, B, H, N, dtype, seed, with_workspace_entry=True, D=64):
     dev = torch.device("cuda")
-    q, k, v = make_qkv(B, H, N, 64, dtype, seed=seed)
+    q, k, v = make_qkv(B, H, N, D, dtype, seed=seed)
     qd, kd, vd = (t.to(dev) for t in (q, k, v))
     o = torch.full_like(vd, float("nan"))
-    S = torch.full((B, H, 64, 64), float("nan"), device=dev)
-    z = torch.full((B, H, 64), float("nan"), device=dev)
+    S = torch.full((B, H, D, D), float("nan"), device=dev)
+    z = torch.full((B, H, D), float("nan"), device=dev)
     rc = _call(so, qd, kd, vd, o, S, z, dtype)
     assert rc == 0, la.la_status_string(rc)
     assert so.la_noalloc_query_status(torch.cuda.current_stream().cuda_stream) == 0
@@ -93,6 +95,20 @@ def test_noalloc_matches_workspace_entry_point_and_oracle(B, H, N, dtype):
     la, so = _lib()
     for seed in (31, 32):
         _check_against_oracle(la, so, B, H, N, dtype, seed)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,N", [(1, 2, 1000), (1, 12, 1024)])
+def test_noalloc_bf16_d128(B, H, N):
+    # (1, 2, 1000): the 128-wide tensor-core path's run sums fit the array.
+    # (1, 12, 1024): 96 chunks, whose run sums and seeds (19 MB) do not; the
+    # fp32 path's 192 chunk states (12.7 MB) do, and that path takes the call.
+    la, so = _lib()
+    # Where the paths differ the final states differ by bf16 rounding, so the
+    # comparison with the workspace entry point is made where both take the
+    # tensor-core path (the same kernels on the same partition).
+    _check_against_oracle(la, so, B, H, N, "bf16", seed=60 + H, D=128,
+                          with_workspace_entry=(H == 2))
 
 
 @pytest.mark.gpu
