@@ -139,6 +139,9 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
  * inclusive prefix sums S_i, z_i. Shapes and dtypes as la_noncausal_fwd.
  * S_out [B,H,Dk,Dv] and z_out [B,H,Dk] (float32, nullable) receive the final
  * state S_N, z_N, so that la_decode_step can continue the sequence.
+ * bf16 with Dk = Dv = 64 runs one fused tensor-core launch; bf16 with
+ * Dk = Dv = 128 three (run sums, a seed scan over them, the output pass);
+ * other shapes and fp32 run fp32 arithmetic on the CUDA cores.
  */
 la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
                         int B, int H, int N, int Dk, int Dv, la_dtype dt, float eps,
@@ -155,7 +158,9 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o,
  * S_i is stored ("Transformers Are RNNs: Linear Attention", "Turn Causal
  * Attention into a Recurrence", on cumulative-sum gradients); then
  * dq = dphi(q) phi'(q) with phi'(x) = 1 for x > 0, e^x for x <= 0.
- *  - fp32 arithmetic for both dtypes; Dk, Dv <= 64 (larger: LA_ERR_UNSUPPORTED).
+ *  - bf16 with Dk = Dv = 64: tensor-core products (bf16 operands, fp32
+ *    accumulation); otherwise fp32 arithmetic. Dk, Dv <= 64 (larger:
+ *    LA_ERR_UNSUPPORTED).
  *  - workspace: la_workspace_size(LA_OP_CAUSAL_BWD, ...) bytes, initialised once
  *    with la_workspace_init.
  */
@@ -171,7 +176,9 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
  * sequence: dphi(q_i) = S dnum_i + z dden_i, dphi(k_j) = R v_j + r,
  * dv_j = R^T phi(k_j) ("Transformers Are RNNs: Linear Attention", the
  * associativity rewrite that shares S and z among all queries).
- *  - fp32 arithmetic for both dtypes; Dk, Dv <= 64 (larger: LA_ERR_UNSUPPORTED).
+ *  - bf16 with Dk = Dv = 64: tensor-core products (bf16 operands, fp32
+ *    accumulation); otherwise fp32 arithmetic. Dk, Dv <= 64 (larger:
+ *    LA_ERR_UNSUPPORTED).
  *  - workspace: la_workspace_size(LA_OP_NONCAUSAL_BWD, ...) bytes, initialised
  *    once with la_workspace_init.
  */
@@ -216,8 +223,11 @@ la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void*
  *  - Shapes whose scratch would exceed 16 MiB return LA_ERR_WORKSPACE and
  *    launch nothing. bf16 with Dk = Dv = 64 needs two tagged state sums per
  *    CTA (about 10 MB on a 152-SM GPU) whatever the shape, so it always fits.
- *    The other paths keep one fp32 state per 64-token chunk: at
- *    Dk = Dv = 64 they fit B*H*ceil(N/64) <= 1008.
+ *    bf16 with Dk = Dv = 128 takes its tensor-core path when that path's run
+ *    sums and seeds (66 KB per CTA range and run) fit, as they do up to 84
+ *    chunks of 128 tokens in all; beyond that the fp32 path takes the call if
+ *    it fits. The fp32 path keeps one fp32 state per 64-token chunk: at
+ *    Dk = Dv = 64 it fits B*H*ceil(N/64) <= 1008.
  *  - All calls share the one array, which keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, or concurrent host
  *    threads without ordering) race on it and must be serialised by the caller.
