@@ -645,7 +645,7 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    if ((err = tc_run_sums128(km, vm, agg, p, N, fm, hdr, st))) return err;
+    if ((err = tc_run_sums128(k, v, agg, BH, N, fm, ws_header, st))) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -50,6 +50,11 @@ int tc_causal_launches(int D);
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                       int D, float eps, int fm, const float* S0, const float* z0, float* S_out,
                       float* z_out, void* ws_header, void* scratch, cudaStream_t st);
+// Per-run sums S_run = phi(K)^T V (Dk = Dv = 128, fp32, feature rows) and z_run
+// over the persistent chunk partition of (BH, N), one slot of D * D + D floats
+// per (CTA, run) at agg + (cta * maxr + run) * (D * D + D) (noncausal_tc.cu).
+cudaError_t tc_run_sums128(const void* k, const void* v, float* agg, int64_t BH, int N, int fm,
+                           void* ws_header, cudaStream_t st);
 size_t tc_causal128_workspace(int64_t BH, int N);
 cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                          float eps, int fm, const float* S0, const float* z0, float* S_out,

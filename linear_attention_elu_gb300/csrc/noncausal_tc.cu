@@ -640,8 +640,13 @@ cudaError_t launch_noncausal(const CUtensorMap& qm, const CUtensorMap& km, const
 
 }  // namespace
 
-cudaError_t tc_run_sums128(const CUtensorMap& kmap, const CUtensorMap& vmap, float* agg,
-                           const Partition& p, int N, int fm, WsHeader* hdr, cudaStream_t st) {
+cudaError_t tc_run_sums128(const void* k, const void* v, float* agg, int64_t BH, int N, int fm,
+                           void* ws_header, cudaStream_t st) {
+    Partition p = make_partition(BH, N, sm_count());
+    CUtensorMap kmap, vmap;
+    if (!encode_bhnd(&kmap, k, BH, N, 128) || !encode_bhnd(&vmap, v, BH, N, 128))
+        return cudaErrorInvalidValue;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     const bool ident = fm == kPhiIdentity;
     auto state_kernel = ident ? nc_state_kernel<128, kPhiIdentity> : nc_state_kernel<128, kPhiElu1>;
     static std::atomic<int> optin[2][kMaxDevices];

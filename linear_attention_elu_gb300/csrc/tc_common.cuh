@@ -229,11 +229,4 @@ inline cudaError_t ensure_smem_optin(Kernel kernel, int bytes, std::atomic<int>*
 }
 
 }  // namespace tcc
-
-// Per-run sums S_run = phi(K)^T V (Dk = Dv = 128, fp32, feature rows) and z_run
-// over the partition `p`, one slot of D * D + D floats per (CTA, run) at
-// agg + (cta * p.maxr + run) * (D * D + D) (noncausal_tc.cu).
-cudaError_t tc_run_sums128(const CUtensorMap& kmap, const CUtensorMap& vmap, float* agg,
-                           const tcc::Partition& p, int N, int fm, WsHeader* hdr, cudaStream_t st);
-
 }  // namespace la
