@@ -191,7 +191,7 @@ la_status la_launch_count(la_op op, int B, int H, int N, int Dk, int Dv, la_dtyp
     else if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD)
         *launches = 5;
     else if (op == LA_OP_CAUSAL && la::tc_causal_supported(Dk, Dv, dt))
-        *launches = la::tc_causal_launches(Dk);
+        *launches = la::tc_causal_launches(Dk, (int64_t)B * H, N);
     else if (op == LA_OP_NONCAUSAL && la::tc_noncausal_supported(Dk, Dv, dt))
         *launches = 2;
     else

@@ -19,7 +19,9 @@
 //   2. c128_seed_kernel: per CTA the state before its first chunk, the head's
 //      initial state plus the sums of that head's runs in the ranges to the
 //      left (an exclusive prefix over segments, same blog, section 7.7, as a
-//      segmented scan over the ranges), fp32;
+//      segmented scan over the ranges), fp32. Where every head spans at most
+//      kWalkMax + 1 ranges, the output kernel sums its own seed instead and this
+//      launch is skipped;
 //   3. c128_out_kernel: each CTA walks its range chunk by chunk. The running
 //      state lives in TMEM as fp32 and is advanced by the state MMA itself
 //      (accumulate); after each chunk a bf16 copy (z as hi + lo) is written to
@@ -51,6 +53,22 @@ constexpr int kE = kD * kD + kD;               // floats per state: S [f][v] row
 // carries are chained, and each warp writes its segment's seeds.
 constexpr int kSeedMaxGrid = 1024;
 constexpr int kSeedWarps = 16;
+// Where no range's first head reaches back over more than this many ranges, the
+// output kernel sums its seed from the run sums itself and the scan is skipped.
+constexpr int kWalkMax = 4;
+
+// Ranges to the left of range c that hold part of its first head (0 when the
+// range starts its head), counted up to kWalkMax + 1.
+__host__ __device__ inline int left_walk(const Partition& p, int c) {
+    const int64_t u0 = p.begin(c), hb = u0 / p.nchunks * p.nchunks;
+    if (u0 == hb) return 0;
+    int w = 0;
+    for (int c2 = c - 1; c2 >= 0 && w <= kWalkMax; --c2) {
+        ++w;
+        if (p.begin(c2) <= hb) break;
+    }
+    return w;
+}
 
 struct RangeInfo {
     int run;          // index of the last run (its slot in the run sums)
@@ -216,7 +234,8 @@ template <bool kInit, int kPhi>
 __global__ void __launch_bounds__(kThreads, 1)
 c128_out_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                const float* __restrict__ seeds, const float* __restrict__ S0,
+                const float* __restrict__ agg, const float* __restrict__ seeds,
+                const float* __restrict__ S0,
                 const float* __restrict__ z0, float* __restrict__ S_out, float* __restrict__ z_out,
                 Partition part, int N, float eps, WsHeader* hdr) {
     extern __shared__ uint8_t smem_raw[];
@@ -502,13 +521,26 @@ c128_out_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const int t = tid - 32 * kStateW0;
         const int f = 32 * q4 + lane;
         const uint32_t ts = tmem + kTmS + lane_base;
-        // Writes state row f (fp32 values x[0..127], z) to TMEM and the operand.
-        auto write_row = [&](auto&& value_at, float z) {
+        // Writes state row f to TMEM and the operand: values row[0..127] (zero when
+        // row is null) plus adds[w][0..127] for w < nadd, and z. Rows are read as
+        // 16-byte pieces, eight in flight per 32 values.
+        auto write_row = [&](const float* row, const float* const* adds, int nadd, float z) {
 #pragma unroll 1
             for (int pc = 0; pc < 4; ++pc) {
                 float x[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = value_at(32 * pc + e);
+                for (int q = 0; q < 8; ++q) {
+                    const float4 a = row ? reinterpret_cast<const float4*>(row + 32 * pc)[q]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[4 * q] = a.x; x[4 * q + 1] = a.y; x[4 * q + 2] = a.z; x[4 * q + 3] = a.w;
+                }
+                for (int w = 0; w < nadd; ++w) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 a = reinterpret_cast<const float4*>(adds[w] + 32 * pc)[q];
+                        x[4 * q] += a.x; x[4 * q + 1] += a.y; x[4 * q + 2] += a.z; x[4 * q + 3] += a.w;
+                    }
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(x[e]);
@@ -529,17 +561,32 @@ c128_out_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             *reinterpret_cast<uint4*>(sop + 2 * kTileBytes + f * 128 + ((0 ^ (f & 7)) << 4)) =
                 make_uint4(pack_bf16(zh, z - zh), 0, 0, 0);
         };
-        auto init_at = [&](int64_t h) {
-            return [=](int idx) -> float { return kInit ? S0[h * kD * kD + (int64_t)f * kD + idx] : 0.f; };
-        };
-        // The seed comes from the scan launch.
+        // The seed comes from the scan launch, or (seeds == nullptr) from the run
+        // sums of the at most kWalkMax ranges to the left that hold this range's
+        // first head, added to that head's initial state.
         pdl_wait();
         bool ok = true;
-        {
+        if (seeds) {
             const float* sd = seeds + (int64_t)cta * kE;
-            write_row([&](int idx) { return sd[f * kD + idx]; }, sd[kD * kD + f]);
-            tmem_st_wait();
+            write_row(sd + f * kD, nullptr, 0, sd[kD * kD + f]);
+        } else {
+            const int64_t h0 = u0 / nchunks, hb = h0 * nchunks;
+            const float* wp[kWalkMax];
+            int nw = 0;
+            if (u0 != hb) {
+                for (int c2 = cta - 1; c2 >= 0 && nw < kWalkMax; --c2) {
+                    const int64_t a0 = part.begin(c2), a1 = part.begin(c2 + 1);
+                    wp[nw++] = agg + ((int64_t)c2 * part.maxr + ((a1 - 1) / nchunks - a0 / nchunks)) * kE;
+                    if (a0 <= hb) break;
+                }
+            }
+            float z = kInit ? z0[h0 * kD + f] : 0.f;
+            for (int w = 0; w < nw; ++w) z += wp[w][kD * kD + f];
+            const float* rows[kWalkMax];
+            for (int w = 0; w < nw; ++w) rows[w] = wp[w] + f * kD;
+            write_row(kInit ? S0 + h0 * kD * kD + (int64_t)f * kD : nullptr, rows, nw, z);
         }
+        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         ok = named_bar_and(kBarState, 128, ok);
@@ -577,9 +624,9 @@ c128_out_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     }
                     if (next) {
                         if constexpr (kInit)
-                            write_row(init_at(h + 1), z0[(h + 1) * kD + f]);
+                            write_row(S0 + (h + 1) * kD * kD + (int64_t)f * kD, nullptr, 0, z0[(h + 1) * kD + f]);
                         else
-                            write_row([](int) { return 0.f; }, 0.f);
+                            write_row(nullptr, nullptr, 0, 0.f);
                         tmem_st_wait();
                     }
                 } else {
@@ -627,6 +674,13 @@ static_assert(kSmem <= 232448, "shared memory exceeds 227 KB");
 
 }  // namespace
 
+int tc_causal128_launches(int64_t BH, int N) {
+    Partition p = make_partition(BH, N, sm_count());
+    int walk = 0;
+    for (int c = 0; c < p.grid && walk <= kWalkMax; ++c) walk = max(walk, left_walk(p, c));
+    return walk <= kWalkMax ? 2 : 3;
+}
+
 size_t tc_causal128_workspace(int64_t BH, int N) {
     Partition p = make_partition(BH, N, sm_count());
     return sizeof(float) * (size_t)p.grid * (p.maxr + 1) * (size_t)kE;
@@ -640,6 +694,9 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     float* agg = reinterpret_cast<float*>(scratch);
     float* seeds = agg + (size_t)p.grid * p.maxr * kE;
+    int walk = 0;
+    for (int c = 0; c < p.grid && walk <= kWalkMax; ++c) walk = max(walk, left_walk(p, c));
+    if (walk <= kWalkMax) seeds = nullptr;     // each range sums its own seed
     CUtensorMap qm, km, vm, om;
     if (!encode_bhnd(&qm, q, BH, N, kD) || !encode_bhnd(&km, k, BH, N, kD) ||
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
@@ -655,7 +712,7 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, c128_seed_kernel, (const float*)agg, seeds, p, S0, z0)))
+    if (seeds && (err = cudaLaunchKernelEx(&cfg, c128_seed_kernel, (const float*)agg, seeds, p, S0, z0)))
         return err;
     using Kernel = decltype(&c128_out_kernel<false, kPhiElu1>);
     static std::atomic<int> optin[4][kMaxDevices];
@@ -666,8 +723,8 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
-    return cudaLaunchKernelEx(&cfg, kernels[variant], qm, km, vm, om, (const float*)seeds, S0, z0,
-                              S_out, z_out, p, N, eps, hdr);
+    return cudaLaunchKernelEx(&cfg, kernels[variant], qm, km, vm, om, (const float*)agg,
+                              (const float*)seeds, S0, z0, S_out, z_out, p, N, eps, hdr);
 }
 
 }  // namespace la

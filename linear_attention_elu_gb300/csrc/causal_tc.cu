@@ -822,7 +822,7 @@ size_t tc_causal_workspace(int64_t BH, int N, int D) {
     return 2 * sizeof(uint64_t) * (size_t)p.grid * kE;
 }
 
-int tc_causal_launches(int D) { return D == 128 ? 3 : 1; }
+int tc_causal_launches(int D, int64_t BH, int N) { return D == 128 ? tc_causal128_launches(BH, N) : 1; }
 
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                       int D, float eps, int fm, const float* S0, const float* z0, float* S_out,

@@ -46,7 +46,7 @@ cudaError_t tc_random_features(const void* x, const void* W, void* out, int64_t 
 // causal_tc.cu) or 128 (run sums, seed scan, output pass: causal128_tc.cu).
 bool tc_causal_supported(int D, int M, la_dtype dt);
 size_t tc_causal_workspace(int64_t BH, int N, int D);
-int tc_causal_launches(int D);
+int tc_causal_launches(int D, int64_t BH, int N);
 cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                       int D, float eps, int fm, const float* S0, const float* z0, float* S_out,
                       float* z_out, void* ws_header, void* scratch, cudaStream_t st);
@@ -56,6 +56,7 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
 cudaError_t tc_run_sums128(const void* k, const void* v, float* agg, int64_t BH, int N, int fm,
                            void* ws_header, cudaStream_t st);
 size_t tc_causal128_workspace(int64_t BH, int N);
+int tc_causal128_launches(int64_t BH, int N);
 cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
                          float eps, int fm, const float* S0, const float* z0, float* S_out,
                          float* z_out, void* ws_header, void* scratch, cudaStream_t st);
