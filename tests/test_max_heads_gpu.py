@@ -35,14 +35,15 @@ def sampled(t):
     return to_f64(t.reshape((-1,) + tuple(t.shape[2:]))[HEADS])
 
 
-@pytest.mark.parametrize("causal,dt,N", [
-    (True, "bf16", 3),       # tensor-core causal: ~431 one-chunk heads per CTA range
-    (True, "f32", 3),        # fp32 path: grid.y = 65535
-    (False, "bf16", 3),      # non-causal at D = 64: tensor-core pair, one-chunk heads
-    (False, "f32", 3),       # non-causal fp32 path
+@pytest.mark.parametrize("causal,dt,N,D", [
+    (True, "bf16", 3, 64),    # tensor-core causal: ~431 one-chunk heads per CTA range
+    (True, "bf16", 3, 128),   # 128-wide causal: ~431 runs per range (4.3 GB of run sums)
+    (True, "f32", 3, 64),     # fp32 path: grid.y = 65535
+    (False, "bf16", 3, 64),   # non-causal at D = 64: tensor-core pair, one-chunk heads
+    (False, "f32", 3, 64),    # non-causal fp32 path
 ])
-def test_forward_at_maximum_head_count(la, causal, dt, N):
-    q, k, v = make_qkv(B, H, N, 64, dt, seed=N)
+def test_forward_at_maximum_head_count(la, causal, dt, N, D):
+    q, k, v = make_qkv(B, H, N, D, dt, seed=N)
     dev = torch.device("cuda")
     fn = la.la_causal_fwd if causal else la.la_noncausal_fwd
     o = fn(q.to(dev), k.to(dev), v.to(dev))
