@@ -223,11 +223,10 @@ la_status la_causal_fwd_state(const void* q, const void* k, const void* v, void*
  *  - Shapes whose scratch would exceed 16 MiB return LA_ERR_WORKSPACE and
  *    launch nothing. bf16 with Dk = Dv = 64 needs two tagged state sums per
  *    CTA (about 10 MB on a 152-SM GPU) whatever the shape, so it always fits.
- *    bf16 with Dk = Dv = 128 takes its tensor-core path when that path's run
- *    sums and seeds (66 KB per CTA range and run) fit, as they do up to 84
- *    chunks of 128 tokens in all; beyond that the fp32 path takes the call if
- *    it fits. The fp32 path keeps one fp32 state per 64-token chunk: at
- *    Dk = Dv = 64 it fits B*H*ceil(N/64) <= 1008.
+ *    bf16 with Dk = Dv = 128 keeps two 66 KB states per CTA range, which fit
+ *    up to 127 chunks of 128 tokens in all (B*H*ceil(N/128) <= 127). The fp32
+ *    path keeps one fp32 state per 64-token chunk: at Dk = Dv = 64 it fits
+ *    B*H*ceil(N/64) <= 1008.
  *  - All calls share the one array, which keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, or concurrent host
  *    threads without ordering) race on it and must be serialised by the caller.

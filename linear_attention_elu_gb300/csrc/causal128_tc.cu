@@ -14,8 +14,11 @@
 // At 128 features a chunk's tiles and accumulators are twice those of the
 // 64-wide fused kernel, so the work is three launches over the persistent chunk
 // partition (each CTA one contiguous range of the head-major chunk sequence):
-//   1. run sums (nc_state_kernel<128>, noncausal_tc.cu): per run (a CTA's
-//      chunks of one head) S_run = phi(K)^T V and z_run, fp32, in the workspace;
+//   1. run sums (nc_state_kernel<128, *, true>, noncausal_tc.cu): S_run =
+//      phi(K)^T V and z_run (fp32) of each range's last run when its head
+//      continues into the next range, the only runs a seed adds up (a range to
+//      the left of range c that holds part of c's first head has it as its
+//      last run); other chunks are not read;
 //   2. c128_seed_kernel: per CTA the state before its first chunk, the head's
 //      initial state plus the sums of that head's runs in the ranges to the
 //      left (an exclusive prefix over segments, same blog, section 7.7, as a
@@ -71,7 +74,6 @@ __host__ __device__ inline int left_walk(const Partition& p, int c) {
 }
 
 struct RangeInfo {
-    int run;          // index of the last run (its slot in the run sums)
     int flags;        // 1: starts its first head; 2: its last head continues
     int h0, hl;       // first and last head
 };
@@ -90,7 +92,6 @@ c128_seed_kernel(const float* __restrict__ agg, float* __restrict__ seeds, Parti
         RangeInfo r;
         r.h0 = (int)(u0 / nch);
         r.hl = (int)((u1 - 1) / nch);
-        r.run = r.hl - r.h0;
         r.flags = (u0 % nch == 0 ? 1 : 0) | (u1 % nch != 0 ? 2 : 0);
         info[c] = r;
     }
@@ -103,9 +104,7 @@ c128_seed_kernel(const float* __restrict__ agg, float* __restrict__ seeds, Parti
         if (!S0 || !live) return 0.f;
         return idx < kD * kD ? S0[(int64_t)h * kD * kD + idx] : z0[(int64_t)h * kD + idx - kD * kD];
     };
-    auto last_sum = [&](int c) -> float {
-        return live ? agg[((int64_t)c * p.maxr + info[c].run) * kE + idx] : 0.f;
-    };
+    auto last_sum = [&](int c) -> float { return live ? agg[(int64_t)c * kE + idx] : 0.f; };
     const int L = (G + kSeedWarps - 1) / kSeedWarps;
     const int c0 = min(G, w * L), c1 = min(G, c0 + L);
     // The last-run sums of 8 ranges are loaded before they are used, so that a
@@ -575,8 +574,8 @@ c128_out_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             int nw = 0;
             if (u0 != hb) {
                 for (int c2 = cta - 1; c2 >= 0 && nw < kWalkMax; --c2) {
-                    const int64_t a0 = part.begin(c2), a1 = part.begin(c2 + 1);
-                    wp[nw++] = agg + ((int64_t)c2 * part.maxr + ((a1 - 1) / nchunks - a0 / nchunks)) * kE;
+                    const int64_t a0 = part.begin(c2);
+                    wp[nw++] = agg + (int64_t)c2 * kE;   // its last run: this range's first head
                     if (a0 <= hb) break;
                 }
             }
@@ -681,9 +680,10 @@ int tc_causal128_launches(int64_t BH, int N) {
     return walk <= kWalkMax ? 2 : 3;
 }
 
+// Workspace after the header: one last-run sum and one seed per CTA.
 size_t tc_causal128_workspace(int64_t BH, int N) {
     Partition p = make_partition(BH, N, sm_count());
-    return sizeof(float) * (size_t)p.grid * (p.maxr + 1) * (size_t)kE;
+    return sizeof(float) * (size_t)p.grid * 2 * (size_t)kE;
 }
 
 cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,
@@ -693,7 +693,7 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
     if (p.grid > kSeedMaxGrid) return cudaErrorInvalidConfiguration;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     float* agg = reinterpret_cast<float*>(scratch);
-    float* seeds = agg + (size_t)p.grid * p.maxr * kE;
+    float* seeds = agg + (size_t)p.grid * kE;
     int walk = 0;
     for (int c = 0; c < p.grid && walk <= kWalkMax; ++c) walk = max(walk, left_walk(p, c));
     if (walk <= kWalkMax) seeds = nullptr;     // each range sums its own seed
@@ -702,7 +702,7 @@ cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, i
         !encode_bhnd(&vm, v, BH, N, kD) || !encode_bhnd(&om, o, BH, N, kD))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    if ((err = tc_run_sums128(k, v, agg, BH, N, fm, ws_header, st))) return err;
+    if ((err = tc_run_sums128(k, v, agg, BH, N, fm, true, ws_header, st))) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -52,9 +52,11 @@ cudaError_t tc_causal(const void* q, const void* k, const void* v, void* o, int6
                       float* z_out, void* ws_header, void* scratch, cudaStream_t st);
 // Per-run sums S_run = phi(K)^T V (Dk = Dv = 128, fp32, feature rows) and z_run
 // over the persistent chunk partition of (BH, N), one slot of D * D + D floats
-// per (CTA, run) at agg + (cta * maxr + run) * (D * D + D) (noncausal_tc.cu).
+// per (CTA, run) at agg + (cta * maxr + run) * (D * D + D); with last_only, only
+// each range's last run when its head continues, at agg + cta * (D * D + D)
+// (noncausal_tc.cu).
 cudaError_t tc_run_sums128(const void* k, const void* v, float* agg, int64_t BH, int N, int fm,
-                           void* ws_header, cudaStream_t st);
+                           bool last_only, void* ws_header, cudaStream_t st);
 size_t tc_causal128_workspace(int64_t BH, int N);
 int tc_causal128_launches(int64_t BH, int N);
 cudaError_t tc_causal128(const void* q, const void* k, const void* v, void* o, int64_t BH, int N,

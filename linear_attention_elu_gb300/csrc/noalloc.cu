@@ -107,9 +107,8 @@ extern "C" la_status la_causal_fwd_noalloc(const void* q, const void* k, const v
     if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return LA_ERR_INVALID_ARG;
     if ((S_out && !aligned16(S_out)) || (z_out && !aligned16(z_out))) return LA_ERR_INVALID_ARG;
-    // Tensor-core path when its workspace fits the array; at Dk = Dv = 128 its run
-    // sums outgrow the array before the fp32 path's chunk states do on short
-    // sequences, so the fp32 path takes what the tensor-core path cannot.
+    // Tensor-core path when its workspace fits the array, else the fp32 path
+    // when its workspace does.
     bool tc = la::tc_causal_supported(Dk, Dv, dt);
     size_t body = tc ? la::tc_causal_workspace(BH, N, Dk) : la::simt_causal_workspace(BH, N, Dk, Dv);
     if (tc && Dk != 64 && kHeaderBytes + body > kNoAllocScratchBytes) {

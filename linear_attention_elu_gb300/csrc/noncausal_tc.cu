@@ -54,7 +54,10 @@ template <int kD> constexpr uint32_t kSOnes = kSStages<kD> * kSStage<kD>;
 template <int kD> constexpr size_t kSSmem = 1024 + kSOnes<kD> + (kD == 64 ? kTileBytes : 0);
 constexpr int kSThreads = 320;
 
-template <int kD, int kPhi>
+// kLast (causal use): only the last run of each range, and only when its head
+// continues into the next range, into slot agg + cta * kE (the run that the
+// ranges to the right add up); other chunks are not read.
+template <int kD, int kPhi, bool kLast = false>
 __global__ void __launch_bounds__(kSThreads, 1)
 nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 float* __restrict__ agg, Partition part, int N, WsHeader* hdr) {
@@ -71,7 +74,10 @@ nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const bool hold = hdr->hold_item != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
-    const int64_t u0 = part.begin(cta), u1 = part.begin(cta + 1);
+    const int64_t u1 = part.begin(cta + 1);
+    const int64_t u0 = !kLast ? part.begin(cta)
+                       : (u1 % part.nchunks == 0 ? u1
+                                                 : max(part.begin(cta), u1 / part.nchunks * part.nchunks));
     auto stage = [&](int s) { return base + s * kSStage<kD>; };
     uint8_t* ones = base + kSOnes<kD>;
 
@@ -218,7 +224,7 @@ nc_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             if (!ok) break;
             if (t == 0) mbar_arrive(&phi_done[s]);
             if (last_in_run) {
-                float* out = agg + ((int64_t)cta * part.maxr + run) * kE<kD>;
+                float* out = agg + (kLast ? (int64_t)cta : (int64_t)cta * part.maxr + run) * kE<kD>;
                 if constexpr (kD == 128) {
                     // z of the run: reduce the column-group partials.
 #pragma unroll
@@ -641,16 +647,17 @@ cudaError_t launch_noncausal(const CUtensorMap& qm, const CUtensorMap& km, const
 }  // namespace
 
 cudaError_t tc_run_sums128(const void* k, const void* v, float* agg, int64_t BH, int N, int fm,
-                           void* ws_header, cudaStream_t st) {
+                           bool last_only, void* ws_header, cudaStream_t st) {
     Partition p = make_partition(BH, N, sm_count());
     CUtensorMap kmap, vmap;
     if (!encode_bhnd(&kmap, k, BH, N, 128) || !encode_bhnd(&vmap, v, BH, N, 128))
         return cudaErrorInvalidValue;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws_header);
     const bool ident = fm == kPhiIdentity;
-    auto state_kernel = ident ? nc_state_kernel<128, kPhiIdentity> : nc_state_kernel<128, kPhiElu1>;
-    static std::atomic<int> optin[2][kMaxDevices];
-    cudaError_t err = ensure_smem_optin(state_kernel, (int)kSSmem<128>, optin[ident]);
+    auto state_kernel = last_only ? (ident ? nc_state_kernel<128, kPhiIdentity, true> : nc_state_kernel<128, kPhiElu1, true>)
+                                  : (ident ? nc_state_kernel<128, kPhiIdentity> : nc_state_kernel<128, kPhiElu1>);
+    static std::atomic<int> optin[2][2][kMaxDevices];
+    cudaError_t err = ensure_smem_optin(state_kernel, (int)kSSmem<128>, optin[last_only][ident]);
     if (err) return err;
     state_kernel<<<p.grid, kSThreads, kSSmem<128>, st>>>(kmap, vmap, agg, p, N, hdr);
     return cudaPeekAtLastError();

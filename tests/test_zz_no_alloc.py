@@ -9,8 +9,8 @@ into a new result. They also run the fp32 path at the array's exact capacity,
 alternate fp32 and bf16 calls (the fp32 path leaves per-chunk fp32 states
 where the bf16 path reads tagged words), make a bounded wait run out through
 the header's test hook and read the status back, and check that host memory
-is refused before any launch, and take the 128-wide bf16 path both where its
-run sums fit the array and where the fp32 path must take the call instead.
+is refused before any launch, and take the 128-wide bf16 path up to the
+largest shape whose last-run sums and seeds fit the array.
 This file is collected last on purpose.
 """
 import ctypes
@@ -98,17 +98,13 @@ def test_noalloc_matches_workspace_entry_point_and_oracle(B, H, N, dtype):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("B,H,N", [(1, 2, 1000), (1, 12, 1024)])
+@pytest.mark.parametrize("B,H,N", [(1, 2, 1000), (1, 1, 127 * 128)])
 def test_noalloc_bf16_d128(B, H, N):
-    # (1, 2, 1000): the 128-wide tensor-core path's run sums fit the array.
-    # (1, 12, 1024): 96 chunks, whose run sums and seeds (19 MB) do not; the
-    # fp32 path's 192 chunk states (12.7 MB) do, and that path takes the call.
+    # The 128-wide tensor-core path keeps one last-run sum and one seed per CTA
+    # (2 x 66,048 bytes): (1, 2, 1000) is 16 chunks; (1, 1, 127 x 128) is 127
+    # chunks on 127 CTAs, the most the array holds (128 is refused below).
     la, so = _lib()
-    # Where the paths differ the final states differ by bf16 rounding, so the
-    # comparison with the workspace entry point is made where both take the
-    # tensor-core path (the same kernels on the same partition).
-    _check_against_oracle(la, so, B, H, N, "bf16", seed=60 + H, D=128,
-                          with_workspace_entry=(H == 2))
+    _check_against_oracle(la, so, B, H, N, "bf16", seed=60 + H, D=128)
 
 
 @pytest.mark.gpu
@@ -173,4 +169,8 @@ def test_noalloc_rejects_shapes_beyond_its_capacity():
     assert f(fake, fake, fake, fake, 8, 8, 65536, 64, 64, LA_F32, 1e-6, None, None, None) \
         == LA_ERR_WORKSPACE
     assert f(fake, fake, fake, fake, 1, 1, 1009 * 64, 64, 64, LA_F32, 1e-6, None, None, None) \
+        == LA_ERR_WORKSPACE
+    # 128 chunks at Dk = Dv = 128: neither the tensor-core path (128 CTAs x two
+    # 66,048-byte states) nor the fp32 path (256 chunk states) fits.
+    assert f(fake, fake, fake, fake, 1, 1, 128 * 128, 128, 128, LA_BF16, 1e-6, None, None, None) \
         == LA_ERR_WORKSPACE
