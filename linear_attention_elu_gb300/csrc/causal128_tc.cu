@@ -12,8 +12,9 @@
 // features as M, and z falls out of the ones column of [V | 1].
 //
 // At 128 features a chunk's tiles and accumulators are twice those of the
-// 64-wide fused kernel, so the work is three launches over the persistent chunk
-// partition (each CTA one contiguous range of the head-major chunk sequence):
+// 64-wide fused kernel, so the work is two or three launches over the
+// persistent chunk partition (each CTA one contiguous range of the head-major
+// chunk sequence):
 //   1. run sums (nc_state_kernel<128, *, true>, noncausal_tc.cu): S_run =
 //      phi(K)^T V and z_run (fp32) of each range's last run when its head
 //      continues into the next range, the only runs a seed adds up (a range to
@@ -29,7 +30,8 @@
 //      state lives in TMEM as fp32 and is advanced by the state MMA itself
 //      (accumulate); after each chunk a bf16 copy (z as hi + lo) is written to
 //      shared memory as the B operand of the next chunk's phi(Q) [S | z].
-// Launches 2 and 3 are programmatic dependents of the launch before them.
+// Launches 2 and 3 are programmatic dependents of the launch before them. The
+// workspace holds one last-run sum and one seed per CTA.
 #include <math.h>
 
 #include "common.cuh"
