@@ -73,9 +73,9 @@ constexpr int kE = kD * kD + kD;               // floats per published sum (S ro
 //   warp 19     TMA producer
 //   warp 23     MMA (2); allocates and frees TMEM
 // MMA (1) of chunk i >= 2 needs phi of chunk i and the output warps' reads of
-// chunk i - 2 (same TMEM buffer): both sides count themselves in on a shared
-// counter and the one that arrives second issues it, so neither waits for a
-// wake-up from the other.
+// chunk i - 2 (same TMEM buffer): both sides count themselves in on a counter
+// of chunk i mod 4 and the one that arrives second issues it, so neither waits
+// for a wake-up from the other.
 // Per chunk i of the range (stage s, TMEM buffer b = i mod 2):
 //   (1) A           = phi(Q) phi(K)^T                     M=128, N=128, K=64
 //   (4) [num | den] = P [V | 1]                            M=128, N=80,  K=128
@@ -123,7 +123,7 @@ struct Misc {
     uint64_t snap_ready[kStages], a_full[2], o_full[2];
     uint64_t a_done, ds_full[2], ds_free[2], drain[4];
     uint32_t tmem_slot;
-    int qk_arrive[2];                          // arrivals for MMA (1), per TMEM buffer
+    int qk_arrive[4];                          // arrivals for MMA (1), per chunk mod 4
     int walk_stop, walk_incl;
 };
 
@@ -242,6 +242,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             mbar_init(&m.a_full[b], 1);
             mbar_init(&m.o_full[b], 1);
             m.qk_arrive[b] = 0;
+            m.qk_arrive[b + 2] = 0;
         }
         for (int d = 0; d < 4; ++d) mbar_init(&m.drain[d], 1);
         mbar_init(&m.a_done, 1);
@@ -286,13 +287,17 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                      smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_qk, k16 > 0);
         mma_commit(&m.a_full[b]);
     };
-    // One of the two arrivals (phi of chunk i, output reads of chunk i - 2) for
-    // MMA (1) of chunk i >= 2 on TMEM buffer b; true for the second one, whose
-    // thread then issues it. Arrivals alternate, so the counter's old value is
+    // One of the two arrivals (phi of chunk i, output reads of chunk i - 2 from
+    // TMEM buffer i mod 2) for MMA (1) of chunk i >= 2, on counter c = i mod 4;
+    // true for the second one, whose thread then issues it. Chunks i and i + 4
+    // share a counter, but the phi side reaches chunk i + 4 only after (3) of
+    // chunk i + 1, hence after the output side counted in for chunk i, and the
+    // output side reaches it only after phi of chunk i + 2: a chunk's two
+    // arrivals are never mixed with another's, so the counter's old value is
     // odd exactly for the second.
-    auto qk_second = [&](int b) -> bool {
+    auto qk_second = [&](int c) -> bool {
         __threadfence_block();
-        const int prev = atomicAdd(&m.qk_arrive[b], 1);
+        const int prev = atomicAdd(&m.qk_arrive[c], 1);
         __threadfence_block();
         return (prev & 1) != 0;
     };
@@ -404,11 +409,9 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
             if (!ok) break;
             if (t == 0) {
                 mbar_arrive(&m.phi_done[s]);
-                // Count in for (1) only once (1) of chunk i - 2 was issued, so that the
-                // two arrivals of one chunk are never mixed with the next chunk's on
-                // the same buffer (the output side cannot run ahead: it waits for (3)).
-                if (i >= 4) ok = mbar_wait(&m.a_full[i & 1], ((i - 2) >> 1) & 1, max_spin);
-                if (ok && (i < 2 || qk_second(i & 1))) issue_qk(i);
+                // Count in for (1) without waiting: the counters (one per chunk mod 4)
+                // keep different chunks' arrivals apart.
+                if (ok && (i < 2 || qk_second(i & 3))) issue_qk(i);
             }
         }
         if (t == 0) {
@@ -678,7 +681,7 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                 ok = named_bar_and(kBarPair + 1, 128, ok);
                 if (!ok) break;
                 if (to_t == 0) {
-                    if (j + 2 < nch && qk_second(bj)) issue_qk(j + 2);
+                    if (j + 2 < nch && qk_second((j + 2) & 3)) issue_qk(j + 2);
                     tma_store_wait_read<0>();             // the staging tile is free again
                 }
                 named_bar(kBarPair + 1, 128);
