@@ -271,15 +271,9 @@ bwd_rows_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 tmem_ld16(tb + 32 * jb, r0);
                 tmem_ld16(tb + 32 * jb + 16, r1);
                 tmem_ld_wait();
-                const int lim = jb == q4 ? lane : 31;
                 uint32_t p[16];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = pack_bf16(2 * e <= lim ? __uint_as_float(r0[2 * e]) : 0.f,
-                                     2 * e + 1 <= lim ? __uint_as_float(r0[2 * e + 1]) : 0.f);
-                    p[8 + e] = pack_bf16(16 + 2 * e <= lim ? __uint_as_float(r1[2 * e]) : 0.f,
-                                         17 + 2 * e <= lim ? __uint_as_float(r1[2 * e + 1]) : 0.f);
-                }
+                if (jb < q4) pack_block32(r0, r1, p);
+                else pack_block32_diag(r0, r1, lane, p);
                 tmem_st16(tb + 16 * jb, p);
             }
             for (int jb = q4 + 1; jb < 4; ++jb) {

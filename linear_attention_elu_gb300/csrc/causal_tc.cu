@@ -593,16 +593,9 @@ causal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     tmem_ld16(tbuf + 32 * j + 16, r1);
                     tmem_ld_wait();
                     // Diagonal block: key 32 q4 + e <= row 32 q4 + lane.
-                    const int lim = j == q4 ? lane : 31;
                     uint32_t p[16];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        p[e] = pack_bf16(2 * e <= lim ? __uint_as_float(r0[2 * e]) : 0.f,
-                                         2 * e + 1 <= lim ? __uint_as_float(r0[2 * e + 1]) : 0.f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        p[8 + e] = pack_bf16(16 + 2 * e <= lim ? __uint_as_float(r1[2 * e]) : 0.f,
-                                             17 + 2 * e <= lim ? __uint_as_float(r1[2 * e + 1]) : 0.f);
+                    if (j < q4) pack_block32(r0, r1, p);
+                    else pack_block32_diag(r0, r1, lane, p);
                     tmem_st16(tbuf + 16 * j, p);
                 }
                 for (int j = q4 + 1; ok && j < 4; ++j) {

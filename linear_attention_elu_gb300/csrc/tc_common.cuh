@@ -50,6 +50,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 
+// One 32-key block of causal scores (r0: keys 0-15, r1: keys 16-31, fp32 bits)
+// to 16 words of packed bf16. Blocks below the diagonal keep every key; the
+// diagonal block keeps keys 0..last (the row's own position in the block) and
+// zeroes the rest. The caller picks the form per block (a warp-uniform choice),
+// so the per-key compares run on the diagonal block only.
+__device__ __forceinline__ void pack_block32(const uint32_t* r0, const uint32_t* r1, uint32_t* p) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        p[e] = pack_bf16(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1]));
+        p[8 + e] = pack_bf16(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1]));
+    }
+}
+
+__device__ __forceinline__ void pack_block32_diag(const uint32_t* r0, const uint32_t* r1, int last,
+                                                  uint32_t* p) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        p[e] = pack_bf16(2 * e <= last ? __uint_as_float(r0[2 * e]) : 0.f,
+                         2 * e + 1 <= last ? __uint_as_float(r0[2 * e + 1]) : 0.f);
+        p[8 + e] = pack_bf16(16 + 2 * e <= last ? __uint_as_float(r1[2 * e]) : 0.f,
+                             17 + 2 * e <= last ? __uint_as_float(r1[2 * e + 1]) : 0.f);
+    }
+}
+
 // phi(x) = max(x, 0) + min(e^x, 1) on two packed bf16 values: equal to x + 1
 // for x > 0 and e^x for x <= 0 (e^x >= 1 exactly when x >= 0).
 // Each bf16 value widens exactly to fp32; t = x * fp32(log2 e) is one fp32
