@@ -74,37 +74,38 @@ __device__ __forceinline__ void pack_block32_diag(const uint32_t* r0, const uint
     }
 }
 
-// phi(x) = max(x, 0) + min(e^x, 1) on two packed bf16 values: equal to x + 1
-// for x > 0 and e^x for x <= 0 (e^x >= 1 exactly when x >= 0).
-// Each bf16 value widens exactly to fp32; t = x * fp32(log2 e) is one fp32
-// product (relative error <= 2^-23; the pair in one packed multiply), 2^t is
-// the fp32 hardware ex2 (which flushes results below 2^-126 to zero), and the
-// pair is rounded once to bf16.
-// max, min and the final add are packed bf16 operations (the add rounds the
-// exact sum once). Error bound, for every bf16 input x >= -87.3: the result
-// is within 2^-8 (+ 1e-5) of phi(x) relative, which is the bf16 rounding of
-// phi itself; below -87.3 the result is 0 (e^x < 1.2e-38 there). A float64
-// emulation over every bf16 input checks this bound in the CPU tests.
-// (t rounded to bf16 before a bf16 ex2 costs fewer instructions, but its
-// error grows with |x|: 3 % near x = -5, 13 % below x = -20.)
+// phi(x) = max(x, 0) + e^min(x, 0) on two packed bf16 values: x + 1 for
+// x > 0 (the exponent is 0, e = 1) and e^x for x <= 0.
+// max(x, 0) and max(-x, 0) are packed bf16 fused multiply-adds with relu
+// (x * (+-1) + 0, exact), which run on the FMA pipe. Each value of max(-x, 0)
+// widens exactly to fp32; t = -max(-x, 0) * fp32(log2 e) = min(x, 0) * log2 e
+// is one fp32 product (relative error <= 2^-23; the pair in one packed
+// multiply), 2^t is the fp32 hardware ex2 (which flushes results below 2^-126
+// to zero), the pair is rounded once to bf16, and the final packed bf16 add
+// rounds the exact sum once. Error bound, for every bf16 input x >= -87.3: the
+// result is within 2^-8 (+ 1e-5) of phi(x) relative, which is the bf16
+// rounding of phi itself; below -87.3 the result is 0 (e^x < 1.2e-38 there).
+// A float64 emulation over every bf16 input checks this bound in the CPU
+// tests. (t rounded to bf16 before a bf16 ex2 costs fewer instructions, but
+// its error grows with |x|: 3 % near x = -5, 13 % below x = -20.)
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-    constexpr float kLog2e = 1.4426950408889634f;
-    constexpr uint32_t kOne = 0x3F803F80u;
-    const float xlo = __uint_as_float(x << 16), xhi = __uint_as_float(x & 0xFFFF0000u);
-    // Both products in one packed fp32 multiply, each rounded as a scalar one.
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    constexpr uint32_t kOne = 0x3F803F80u, kMinusOne = 0xBF80BF80u;
+    uint32_t n, p;
+    asm("fma.rn.relu.bf16x2 %0, %1, %2, %3;" : "=r"(n) : "r"(x), "r"(kMinusOne), "r"(0u));
+    asm("fma.rn.relu.bf16x2 %0, %1, %2, %3;" : "=r"(p) : "r"(x), "r"(kOne), "r"(0u));
+    const float nlo = __uint_as_float(n << 16), nhi = __uint_as_float(n & 0xFFFF0000u);
     uint64_t xx, cc, tt;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(xlo), "f"(xhi));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(kLog2e));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(nlo), "f"(nhi));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(kNegLog2e));
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(tt) : "l"(xx), "l"(cc));
     float tlo, thi, elo, ehi;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(tlo), "=f"(thi) : "l"(tt));
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(elo) : "f"(tlo));
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ehi) : "f"(thi));
-    uint32_t e, m, p, r;
+    uint32_t e, r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(e) : "f"(ehi), "f"(elo));
-    asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(e), "r"(kOne));
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(x), "r"(0u));
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(m));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(e));
     return r;
 }
 

@@ -2,10 +2,11 @@
 
 The tensor-core kernels apply phi(x) = elu(x) + 1 ("Why Replace Attention?",
 section 5.3, the boxed map) to bf16 tiles in shared memory:
-    t = fp32(x) * fp32(log2 e)         (one fp32 product)
+    n = max(-x, 0), p = max(x, 0)       (packed bf16 fma with relu, exact)
+    t = fp32(n) * fp32(-log2 e)         (one fp32 product: min(x, 0) log2 e)
     e = ex2.approx.ftz.f32(t)           (fp32 hardware 2^t; results below 2^-126 -> 0)
     e = bf16_rn(e)                      (cvt.rn.bf16x2.f32)
-    phi = bf16_rn(max(x, 0) + min(e, 1))  (packed bf16 max, min and add)
+    phi = bf16_rn(p + e)                (packed bf16 add)
 This file runs those steps in float64 over every finite bf16 input. The fp32
 ex2 is modelled as 2^t within a relative error of 2^-21 in either direction
 (bf16 rounding is monotone, so both ends of that interval bound the result),
@@ -43,17 +44,30 @@ def phi_exact(x):
     return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
 
 
+def ex2_model(t, ex2_scale):
+    """fp32 hardware 2^t (result scaled by ex2_scale), flushed to 0 below 2^-126, then bf16."""
+    e = np.exp2(t) * ex2_scale
+    e = np.where(np.exp2(t) < 2.0 ** -126, 0.0, e)
+    return bf16_rn(e)
+
+
 def phi_kernel(x64, x32, ex2_scale):
     """The kernel's steps with the fp32 ex2 result scaled by ex2_scale."""
-    with np.errstate(over="ignore"):                # huge x: t = inf, min(e, 1) = 1
-        t = (x32 * LOG2E_F32).astype(np.float64)   # fp32 product, rounded once
-    t = np.minimum(t, 1.0)                          # t > 0 only feeds min(e, 1) = 1
-    e = np.exp2(t) * ex2_scale
-    e = np.where(np.exp2(t) < 2.0 ** -126, 0.0, e)  # ftz
-    e = bf16_rn(e)
-    m = np.minimum(e, 1.0)
+    n32 = np.maximum(-x32, np.float32(0.0))         # relu(-x), exact in bf16
+    with np.errstate(over="ignore"):                # huge -x: t = -inf, e = 0
+        t = (n32 * -LOG2E_F32).astype(np.float64)   # fp32 product, rounded once
+    e = ex2_model(t, ex2_scale)
     p = np.maximum(x64, 0.0)
-    return bf16_rn(p + m)
+    return bf16_rn(p + e)
+
+
+def phi_min_max_form(x64, x32, ex2_scale):
+    """The same map as max(x, 0) + min(e^x, 1), e^x of the whole input."""
+    with np.errstate(over="ignore"):                # huge x: t = inf, min(e, 1) = 1
+        t = (x32 * LOG2E_F32).astype(np.float64)
+    t = np.minimum(t, 1.0)                          # t > 0 only feeds min(e, 1) = 1
+    m = np.minimum(ex2_model(t, ex2_scale), 1.0)
+    return bf16_rn(np.maximum(x64, 0.0) + m)
 
 
 def phi_old_design(x64):
@@ -92,6 +106,15 @@ def test_phi_within_stated_bound_over_every_bf16_input():
     assert worst <= BOUND, worst
     # The bound is the bf16 rounding of phi itself: nothing tighter holds.
     assert worst > 2.0 ** -8 * 0.99
+
+
+def test_relu_form_equals_min_max_form_on_every_bf16_input():
+    # exp of min(x, 0) against min(exp(x), 1): the same bits for every finite input,
+    # at both ends of the modelled ex2 error as well.
+    x64, x32 = all_bf16()
+    for scale in (1.0 - EX2_REL, 1.0, 1.0 + EX2_REL):
+        np.testing.assert_array_equal(phi_kernel(x64, x32, scale),
+                                      phi_min_max_form(x64, x32, scale))
 
 
 def test_phi_special_values():
