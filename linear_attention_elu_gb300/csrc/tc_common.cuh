@@ -138,6 +138,20 @@ __device__ __forceinline__ void report_timeout(WsHeader* hdr) {
     atomicCAS(&hdr->status, 0u, (uint32_t)LA_ERR_TIMEOUT);
 }
 
+// Rows >= zero_from of a 128 x 64 bf16 tile set to 0, for the rows
+// (t >> 3) + 32 k, physical chunk (t & 7), that thread t of a 256-thread group
+// owns in the phi loops below. Only a sequence's last, ragged chunk needs it;
+// the phi loops map every row and the owner then overwrites its own rows past
+// the end (program order), so full chunks carry no per-row selects.
+__device__ __forceinline__ void zero_rows_256(uint8_t* tile, int t, int zero_from) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = (t >> 3) + 32 * k;
+        if (r >= zero_from)
+            *reinterpret_cast<uint4*>(tile + r * 128 + (t & 7) * 16) = make_uint4(0, 0, 0, 0);
+    }
+}
+
 // phi in place on the 128 x 64 bf16 tile rows (t >> 3) + 32 k, physical chunk
 // (t & 7), for a 256-thread group; rows >= zero_from are set to 0.
 template <int kPhi = kPhiElu1>
@@ -147,11 +161,10 @@ __device__ __forceinline__ void phi_tile_256(uint8_t* tile, int t, int zero_from
     for (int k = 0; k < 4; ++k)
         v[k] = *reinterpret_cast<const uint4*>(tile + ((t >> 3) + 32 * k) * 128 + (t & 7) * 16);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int r = (t >> 3) + 32 * k;
-        const uint4 o = r < zero_from ? phi8<kPhi>(v[k]) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(tile + r * 128 + (t & 7) * 16) = o;
-    }
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(tile + ((t >> 3) + 32 * k) * 128 + (t & 7) * 16) =
+            phi8<kPhi>(v[k]);
+    if (zero_from < kC) zero_rows_256(tile, t, zero_from);
 }
 
 // phi_tile_256 on two tiles at once, four 16-byte pieces per iteration (all
@@ -175,11 +188,12 @@ __device__ __forceinline__ void phi_tiles2_256(uint8_t* ta, int zero_a, uint8_t*
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int k = k2 + u;
-            const int r = (t >> 3) + 32 * (k & 3);
-            *reinterpret_cast<uint4*>((k < 4 ? ta : tb) + r * 128 + (t & 7) * 16) =
-                r < (k < 4 ? zero_a : zero_b) ? phi8<kPhi>(v[u]) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>((k < 4 ? ta : tb) + ((t >> 3) + 32 * (k & 3)) * 128 +
+                                      (t & 7) * 16) = phi8<kPhi>(v[u]);
         }
     }
+    if (zero_a < kC) zero_rows_256(ta, t, zero_a);
+    if (zero_b < kC) zero_rows_256(tb, t, zero_b);
 }
 
 // The "ones" operand tile: 128 rows, logical column 0 = 1.0, the rest 0.
