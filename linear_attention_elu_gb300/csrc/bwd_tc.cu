@@ -505,34 +505,53 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         ph ^= 1;
         tc_fence_after();
         // Row i, keys 64 hh .. 64 hh + 63: G_ij = acc + dd_i and W_ij = acc for
-        // j <= i (zero otherwise), bf16 into tile hh of G and of W.
+        // j <= i (zero otherwise), bf16 into tile hh of G and of W. Key block
+        // kb = 2 hh + h2 against the warp's rows 32 q4 .. 32 q4 + 31 is below the
+        // diagonal (kb < q4: every key kept), the diagonal block (kb == q4: key
+        // 32 kb + col kept for col <= lane) or above it (zeros, no TMEM read),
+        // the same for the whole warp. Rows past a ragged end (i >= valid) are 0.
         if (ok) {
             const float ddi = m.dd[i];
+            const bool live_row = i < valid;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 uint8_t* dst = (which == 0 ? tG : tW) + hh * kTileBytes;
                 const uint32_t ta = tmem + lane_base + (which == 0 ? 0u : kTmW) + 64 * hh;
+                const float add = which == 0 ? ddi : 0.f;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t r[2][16];
-                    tmem_ld16(ta + 32 * h2, r[0]);
-                    tmem_ld16(ta + 32 * h2 + 16, r[1]);
-                    tmem_ld_wait();
+                    const int kb = 2 * hh + h2;
+                    uint32_t w[16];
+                    if (kb > q4) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t w[4];
+                        for (int e = 0; e < 16; ++e) w[e] = 0u;
+                    } else {
+                        uint32_t r[2][16];
+                        tmem_ld16(ta + 32 * h2, r[0]);
+                        tmem_ld16(ta + 32 * h2 + 16, r[1]);
+                        tmem_ld_wait();
+                        if (kb < q4) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int col = 8 * c8 + 2 * e;          // 0..31 within this half
-                            const int j = 64 * hh + 32 * h2 + col;
-                            const float add = which == 0 ? ddi : 0.f;
-                            const float a = (j <= i && i < valid) ? __uint_as_float(r[col >> 4][col & 15]) + add : 0.f;
-                            const float b = (j + 1 <= i && i < valid) ? __uint_as_float(r[(col + 1) >> 4][(col + 1) & 15]) + add : 0.f;
-                            w[e] = pack_bf16(a, b);
+                            for (int e = 0; e < 16; ++e)
+                                w[e] = pack_bf16(__uint_as_float(r[e >> 3][2 * (e & 7)]) + add,
+                                                 __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                w[e] = pack_bf16(
+                                    2 * e <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7)]) + add : 0.f,
+                                    2 * e + 1 <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add
+                                                      : 0.f);
                         }
-                        *reinterpret_cast<uint4*>(dst + sw128_offset(i, 32 * h2 + 8 * c8)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                        if (!live_row) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) w[e] = 0u;
+                        }
                     }
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4*>(dst + sw128_offset(i, 32 * h2 + 8 * c8)) =
+                            make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
                 }
             }
         }
