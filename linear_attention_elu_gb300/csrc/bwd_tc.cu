@@ -401,43 +401,53 @@ bwd_rows_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 }
 
 // ------------------------------------------------------------ gradient kernel
-// Shared memory: Q, K, V, dnum, S_prev [d][m] and R_next [d][m] (64-row tiles),
-// and for the causal kernel G and W (two tiles each: keys 0..63, 64..127).
+// Shared memory (dynamic only, so that its base is 1024-aligned without slack):
+// Q, K, V, dnum, S_prev [d][m] and R_next [d][m] (64-row tiles); for the causal
+// kernel one G/W buffer (two tiles: keys 0..63, 64..127) that holds W, then G;
+// then the barriers, the TMEM address and z_prev, r_next.
 constexpr uint32_t kGQ = 0, kGK = kTileBytes, kGV = 2 * kTileBytes, kGDn = 3 * kTileBytes;
-constexpr uint32_t kGS = 4 * kTileBytes, kGR = kGS + kD * 128, kGG = kGR + kD * 128;
-constexpr uint32_t kGW = kGG + 2 * kTileBytes;
-template <bool kCausal> constexpr size_t kGradSmem = 1024 + (kCausal ? kGW + 2 * kTileBytes : kGG);
-// TMEM columns. Causal: G 0..127, W 128..255, dphi(q) 256, dphi(k) 320, dv 384
-// (512 allocated, one CTA per SM). Non-causal: dphi(q) 0, dphi(k) 64, dv 128
-// (256 allocated, two CTAs per SM).
-template <bool kCausal> constexpr uint32_t kTmGrad = kCausal ? 256 : 0;
-template <bool kCausal> constexpr uint32_t kTmAlloc = kCausal ? 512 : 256;
-constexpr uint32_t kTmW = 128;
+constexpr uint32_t kGS = 4 * kTileBytes, kGR = kGS + kD * 128, kGB = kGR + kD * 128;
+template <bool kCausal> constexpr uint32_t kGMisc = kCausal ? kGB + 2 * kTileBytes : kGB;
 
 struct GradMisc {
     uint64_t ld, mma;
-    uint32_t tmem_slot;
-    float dd[kC], zp[kD], rn[kD];
+    uint32_t tmem_slot, pad;
+    float zp[kD], rn[kD];
 };
+template <bool kCausal> constexpr size_t kGradSmem = kGMisc<kCausal> + sizeof(GradMisc);
+
+// TMEM columns, 256 allocated in both forms (two CTAs per SM). Causal, in three
+// product phases: (a) W at 0..127, dv at 128, dphi(q) at 192; (b) dv += W^T dnum,
+// G at 0..127 (W already read out); (c) dphi(k) at 0 (G already read out),
+// dphi(q) += G phi(K). Non-causal: dphi(q) 0, dphi(k) 64, dv 128.
+template <bool kCausal> constexpr uint32_t kTmDqG = kCausal ? 192 : 0;
+template <bool kCausal> constexpr uint32_t kTmDkG = kCausal ? 0 : 64;
+constexpr uint32_t kTmDvG = 128, kTmAllocG = 256;
 
 template <bool kCausal, int kPhi>
-__global__ void __launch_bounds__(kBThreads, kCausal ? 1 : 2)
+__global__ void __launch_bounds__(kBThreads, 2)
 bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap dnmap,
                    const float* __restrict__ states, const float* __restrict__ rstates,
                    const float* __restrict__ dd_in, __nv_bfloat16* __restrict__ dq,
                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N,
                    WsHeader* hdr) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ GradMisc m;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // With no static shared memory the dynamic base is 1024-aligned, which the
+    // 128-byte swizzle needs; if it ever is not, report it and touch nothing.
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicCAS(&hdr->status, 0u, (uint32_t)LA_ERR_CUDA);
+        return;
+    }
+    uint8_t* base = smem_raw;
+    GradMisc& m = *reinterpret_cast<GradMisc*>(base + kGMisc<kCausal>);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, nch = gridDim.x;
     const int64_t bh = blockIdx.y;
     const int t0 = c * kC;
     const int valid = min(kC, N - t0);
     uint8_t *tQ = base + kGQ, *tK = base + kGK, *tV = base + kGV, *tDn = base + kGDn;
-    uint8_t *tG = base + kGG, *tW = base + kGW, *tS = base + kGS, *tR = base + kGR;
+    uint8_t *tB = base + kGB, *tS = base + kGS, *tR = base + kGR;
 
     if (tid == 0) {
         mbar_init(&m.ld, 1);
@@ -445,14 +455,14 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&m.tmem_slot, kTmAlloc<kCausal>);
+        tmem_alloc(&m.tmem_slot, kTmAllocG);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = m.tmem_slot;
-    const uint32_t kTmDq = kTmGrad<kCausal>, kTmDk = kTmDq + 64, kTmDv = kTmDq + 128;
+    constexpr uint32_t kTmDq = kTmDqG<kCausal>, kTmDk = kTmDkG<kCausal>, kTmDv = kTmDvG;
     const uint32_t max_spin = hdr->max_spin;
     const bool hold = hdr->hold_item != 0;
     if (tid == 0 && !hold) {
@@ -462,7 +472,7 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         tma_load_3d(tV, &vmap, &m.ld, 0, t0, (int)bh);
         tma_load_3d(tDn, &dnmap, &m.ld, 0, t0, (int)bh);
     }
-    // S_prev and R_next as stored ([d][m]: rows d, columns m), z_prev, r_next, dd.
+    // S_prev and R_next as stored ([d][m]: rows d, columns m), z_prev, r_next.
     const float* sp = states + ((int64_t)bh * nch + (kCausal ? c : 0)) * kE;
     const float* rp = rstates + ((int64_t)bh * nch + (kCausal ? c : 0)) * kE;
     state_rows_to_tile(tS, sp, false, tid);
@@ -471,7 +481,11 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         m.zp[tid] = sp[kD * kD + tid];
         m.rn[tid] = rp[kD * kD + tid];
     }
-    if (tid < kC) m.dd[tid] = tid < valid ? dd_in[(int64_t)bh * N + t0 + tid] : 0.f;
+    const int q4 = warp & 3, hh = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int i = 32 * q4 + lane;                 // this thread's row (query i or key j)
+    const bool live_row = i < valid;
+    const float ddi = live_row ? dd_in[(int64_t)bh * N + t0 + i] : 0.f;
     bool ok = hold ? false : mbar_wait(&m.ld, 0, max_spin);
     if (ok) {
         phi_tile_256<kPhi>(tQ, tid, valid);
@@ -481,131 +495,149 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     tc_fence_before();
     ok = __syncthreads_and(ok);
     tc_fence_after();
-    const int q4 = warp & 3, hh = warp >> 2;
-    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    const int i = 32 * q4 + lane;                 // this thread's row (query i or key j)
     uint32_t ph = 0;
-    if (kCausal) {
-        // G = dnum V^T and W = phi(Q) phi(K)^T (both 128 x 128, K = 64).
-        if (tid == 0 && ok) {
-            const uint32_t id = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t dna = smem_u32(tDn), va = smem_u32(tV), qa = smem_u32(tQ), ka = smem_u32(tK);
-#pragma unroll
-            for (int k16 = 0; k16 < kD / 16; ++k16)
-                mma_bf16(tmem, smem_desc(dna + k16 * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(va + k16 * 32, 16, 1024, kSwizzle128B), id, k16 > 0);
-#pragma unroll
-            for (int k16 = 0; k16 < kD / 16; ++k16)
-                mma_bf16(tmem + kTmW, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id, k16 > 0);
-            mma_commit(&m.mma);
-        }
-        if (ok) ok = mbar_wait(&m.mma, ph, max_spin);
-        ok = __syncthreads_and(ok);
-        ph ^= 1;
-        tc_fence_after();
-        // Row i, keys 64 hh .. 64 hh + 63: G_ij = acc + dd_i and W_ij = acc for
-        // j <= i (zero otherwise), bf16 into tile hh of G and of W. Key block
-        // kb = 2 hh + h2 against the warp's rows 32 q4 .. 32 q4 + 31 is below the
-        // diagonal (kb < q4: every key kept), the diagonal block (kb == q4: key
-        // 32 kb + col kept for col <= lane) or above it (zeros, no TMEM read),
-        // the same for the whole warp. Rows past a ragged end (i >= valid) are 0.
-        if (ok) {
-            const float ddi = m.dd[i];
-            const bool live_row = i < valid;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                uint8_t* dst = (which == 0 ? tG : tW) + hh * kTileBytes;
-                const uint32_t ta = tmem + lane_base + (which == 0 ? 0u : kTmW) + 64 * hh;
-                const float add = which == 0 ? ddi : 0.f;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int kb = 2 * hh + h2;
-                    uint32_t w[16];
-                    if (kb > q4) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) w[e] = 0u;
-                    } else {
-                        uint32_t r[2][16];
-                        tmem_ld16(ta + 32 * h2, r[0]);
-                        tmem_ld16(ta + 32 * h2 + 16, r[1]);
-                        tmem_ld_wait();
-                        if (kb < q4) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                w[e] = pack_bf16(__uint_as_float(r[e >> 3][2 * (e & 7)]) + add,
-                                                 __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                w[e] = pack_bf16(
-                                    2 * e <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7)]) + add : 0.f,
-                                    2 * e + 1 <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add
-                                                      : 0.f);
-                        }
-                        if (!live_row) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) w[e] = 0u;
-                        }
-                    }
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4*>(dst + sw128_offset(i, 32 * h2 + 8 * c8)) =
-                            make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
-    // The three gradients.
-    if (tid == 0 && ok) {
-        const uint32_t qa = smem_u32(tQ), ka = smem_u32(tK), va = smem_u32(tV), dna = smem_u32(tDn);
-        const uint32_t sa = smem_u32(tS), ra = smem_u32(tR), ga = smem_u32(tG), wa = smem_u32(tW);
-        const uint32_t id_kk = idesc_bf16_f32(128, 64, false, false);
-        const uint32_t id_km = idesc_bf16_f32(128, 64, false, true);
-        const uint32_t id_mm = idesc_bf16_f32(128, 64, true, true);
-        // dphi(q) = dnum S_prev^T (+ G phi(K)): B = S [d][m] K-major (N = d, K = m).
+    const uint32_t id_kk = idesc_bf16_f32(128, 64, false, false);
+    const uint32_t id_km = idesc_bf16_f32(128, 64, false, true);
+    const uint32_t id_mm = idesc_bf16_f32(128, 64, true, true);
+    const uint32_t qa = smem_u32(tQ), ka = smem_u32(tK), va = smem_u32(tV), dna = smem_u32(tDn);
+    const uint32_t sa = smem_u32(tS), ra = smem_u32(tR), ba = smem_u32(tB);
+    // dphi(q) = dnum S_prev^T (+ G phi(K)): B = S [d][m] K-major (N = d, K = m).
+    auto issue_dq_base = [&]() {
 #pragma unroll
         for (int k16 = 0; k16 < kD / 16; ++k16)
             mma_bf16(tmem + kTmDq, smem_desc(dna + k16 * 32, 16, 1024, kSwizzle128B),
                      smem_desc(sa + k16 * 32, 16, 1024, kSwizzle128B), id_kk, k16 > 0);
-        // dphi(k) = V R_next^T (+ G^T phi(Q)): B = R [d][m] K-major.
+    };
+    // dphi(k) = V R_next^T (+ G^T phi(Q)): B = R [d][m] K-major.
+    auto issue_dk_base = [&]() {
 #pragma unroll
         for (int k16 = 0; k16 < kD / 16; ++k16)
             mma_bf16(tmem + kTmDk, smem_desc(va + k16 * 32, 16, 1024, kSwizzle128B),
                      smem_desc(ra + k16 * 32, 16, 1024, kSwizzle128B), id_kk, k16 > 0);
-        // dv = phi(K) R_next (+ W^T dnum): B = R [d][m] MN-major (K = d rows, N = m).
+    };
+    // dv = phi(K) R_next (+ W^T dnum): B = R [d][m] MN-major (K = d rows, N = m).
+    auto issue_dv_base = [&]() {
 #pragma unroll
         for (int k16 = 0; k16 < kD / 16; ++k16)
             mma_bf16(tmem + kTmDv, smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B),
                      smem_desc(ra + k16 * 2048, 1024, 1024, kSwizzle128B), id_km, k16 > 0);
-        if (kCausal) {
+    };
+    // The MMAs issued so far complete; every thread then sees their results.
+    auto wait_mma = [&]() {
+        if (ok) ok = mbar_wait(&m.mma, ph, max_spin);
+        ok = __syncthreads_and(ok);
+        ph ^= 1;
+        tc_fence_after();
+    };
+    if constexpr (kCausal) {
+        // Row i, keys 64 hh .. 64 hh + 63 of the 128 x 128 product at TMEM column
+        // 0 (+ add for G), kept for j <= i and zero otherwise, bf16 into tile hh of
+        // the G/W buffer. Key block kb = 2 hh + h2 against the warp's rows
+        // 32 q4 .. 32 q4 + 31 is below the diagonal (kb < q4: every key kept), the
+        // diagonal block (kb == q4: key 32 kb + col kept for col <= lane) or above
+        // it (zeros, no TMEM read), the same for the whole warp. Rows past a
+        // ragged end (i >= valid) are 0.
+        auto masked_to_buffer = [&](float add) {
+            uint8_t* dst = tB + hh * kTileBytes;
+            const uint32_t ta = tmem + lane_base + 64 * hh;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int kb = 2 * hh + h2;
+                uint32_t w[16];
+                if (kb > q4) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w[e] = 0u;
+                } else {
+                    uint32_t r[2][16];
+                    tmem_ld16(ta + 32 * h2, r[0]);
+                    tmem_ld16(ta + 32 * h2 + 16, r[1]);
+                    tmem_ld_wait();
+                    if (kb < q4) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16(__uint_as_float(r[e >> 3][2 * (e & 7)]) + add,
+                                             __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16(
+                                2 * e <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7)]) + add : 0.f,
+                                2 * e + 1 <= lane ? __uint_as_float(r[e >> 3][2 * (e & 7) + 1]) + add
+                                                  : 0.f);
+                    }
+                    if (!live_row) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) w[e] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    *reinterpret_cast<uint4*>(dst + sw128_offset(i, 32 * h2 + 8 * c8)) =
+                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        };
+        const uint32_t id_sq = idesc_bf16_f32(128, 128, false, false);
+        // (a) W = phi(Q) phi(K)^T (128 x 128, K = 64), with the base terms of dv
+        // and dphi(q), whose columns are free.
+        if (tid == 0 && ok) {
+#pragma unroll
+            for (int k16 = 0; k16 < kD / 16; ++k16)
+                mma_bf16(tmem, smem_desc(qa + k16 * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(ka + k16 * 32, 16, 1024, kSwizzle128B), id_sq, k16 > 0);
+            issue_dv_base();
+            issue_dq_base();
+            mma_commit(&m.mma);
+        }
+        wait_mma();
+        if (ok) masked_to_buffer(0.f);
+        // (b) dv += W^T dnum (A = W MN-major, B = dnum MN-major), and
+        // G = dnum V^T into W's columns.
+        if (tid == 0 && ok) {
+#pragma unroll
+            for (int k16 = 0; k16 < kC / 16; ++k16)
+                mma_bf16(tmem + kTmDv, smem_desc(ba + k16 * 2048, kTileBytes, 1024, kSwizzle128B),
+                         smem_desc(dna + k16 * 2048, 1024, 1024, kSwizzle128B), id_mm, 1u);
+#pragma unroll
+            for (int k16 = 0; k16 < kD / 16; ++k16)
+                mma_bf16(tmem, smem_desc(dna + k16 * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(va + k16 * 32, 16, 1024, kSwizzle128B), id_sq, k16 > 0);
+            mma_commit(&m.mma);
+        }
+        wait_mma();                                   // also: W^T dnum has read the buffer
+        if (ok) masked_to_buffer(ddi);
+        // (c) dphi(k) = V R_next^T into G's first columns, then + G^T phi(Q);
+        // dphi(q) += G phi(K).
+        if (tid == 0 && ok) {
+            issue_dk_base();
 #pragma unroll
             for (int k16 = 0; k16 < kC / 16; ++k16) {
                 // + G phi(K): A = G K-major (keys in two tiles), B = phi(K) MN-major.
                 mma_bf16(tmem + kTmDq,
-                         smem_desc(ga + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
+                         smem_desc(ba + (k16 >> 2) * kTileBytes + (k16 & 3) * 32, 16, 1024, kSwizzle128B),
                          smem_desc(ka + k16 * 2048, 1024, 1024, kSwizzle128B), id_km, 1u);
                 // + G^T phi(Q): A = G MN-major (M = keys, two atoms), B = phi(Q) MN-major.
-                mma_bf16(tmem + kTmDk, smem_desc(ga + k16 * 2048, kTileBytes, 1024, kSwizzle128B),
+                mma_bf16(tmem + kTmDk, smem_desc(ba + k16 * 2048, kTileBytes, 1024, kSwizzle128B),
                          smem_desc(qa + k16 * 2048, 1024, 1024, kSwizzle128B), id_mm, 1u);
-                // + W^T dnum: A = W MN-major, B = dnum MN-major.
-                mma_bf16(tmem + kTmDv, smem_desc(wa + k16 * 2048, kTileBytes, 1024, kSwizzle128B),
-                         smem_desc(dna + k16 * 2048, 1024, 1024, kSwizzle128B), id_mm, 1u);
             }
+            mma_commit(&m.mma);
         }
-        mma_commit(&m.mma);
+        wait_mma();
+    } else {
+        if (tid == 0 && ok) {
+            issue_dq_base();
+            issue_dk_base();
+            issue_dv_base();
+            mma_commit(&m.mma);
+        }
+        wait_mma();
     }
-    if (ok) ok = mbar_wait(&m.mma, ph, max_spin);
-    ok = __syncthreads_and(ok);
-    tc_fence_after();
     // Epilogue: row i, columns 32 hh .. 32 hh + 31 of each gradient.
     {
-        const bool live = i < valid && ok;
-        const float ddi = m.dd[i];
+        const bool live = live_row && ok;
         const int64_t row = (int64_t)bh * N + t0 + i;
 #pragma unroll 1
         for (int which = 0; which < 3; ++which) {
@@ -652,13 +684,15 @@ bwd_grad_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmAlloc<kCausal>);
+        tmem_dealloc(tmem, kTmAllocG);
     }
 }
 
 static_assert(kRowsSmem <= 232448 / 2 - 1024, "two rows CTAs per SM");
-static_assert(kGradSmem<true> <= 232448, "gradient kernel shared memory exceeds 227 KB");
-static_assert(kGradSmem<false> <= 232448 / 2 - 2048, "two non-causal gradient CTAs per SM");
+// Two gradient CTAs per SM: each takes its dynamic shared memory plus the 1 KB
+// the system reserves per CTA, out of the SM's 228 KB.
+static_assert(2 * (kGradSmem<true> + 1024) <= 233472, "two causal gradient CTAs per SM");
+static_assert(2 * (kGradSmem<false> + 1024) <= 233472, "two non-causal gradient CTAs per SM");
 
 template <bool kCausal, int kPhi>
 cudaError_t launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
