@@ -24,8 +24,9 @@
 //   epilogue: dnum, dd (to shared memory and global),
 //   (3) [dR^T ; dr] = [dnum | dd]^T phi(Q)  (the chunk's reverse-sum term);
 // simt.cu's reverse scan sums (3) over later chunks; bwd_grad_tc_kernel, one
-// CTA per chunk, forms G and W (bf16, shared memory) and the three gradients as
-// tcgen05 products with fp32 accumulators in TMEM. Operands are 128 x 64 bf16
+// CTA per chunk and two CTAs per SM, forms W and then G (bf16, one shared
+// buffer) and the three gradients as tcgen05 products with fp32 accumulators
+// in TMEM (256 columns). Operands are 128 x 64 bf16
 // tiles with the 128-byte swizzle; a tile of rows r and columns c serves as a
 // K-major operand (K = c) or an MN-major one (K = r), so no transposes are
 // written.
